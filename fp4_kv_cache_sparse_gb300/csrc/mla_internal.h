@@ -1,0 +1,54 @@
+// mla_internal.h -- host/device interface between the C-ABI layer and the
+// kernels of the library (not installed, not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+// Everything the decode kernel reads, resolved by the host layer.
+struct DecodeParams {
+  const uint16_t* q;        // bf16 [nq][h_q][512]
+  const uint8_t* kv;        // FP8 records
+  const int32_t* idx;       // [nq][topk]
+  const uint8_t* xkv;       // FP4 records (extra cache) or null
+  const int32_t* xidx;      // [nq][xtopk] or null
+  const int32_t* sched;     // [num_parts][8]
+  const int32_t* num_splits;  // [nq + 1]
+  float* ws_o;              // [ws_splits_cap][h_q][512]
+  float* ws_lse;            // [ws_splits_cap][h_q]
+  int64_t ws_splits_cap;
+  uint16_t* out;            // bf16 [nq][h_q][512]
+  float* lse;               // [nq][h_q]
+  int32_t* d_error;         // nullable
+  int nq, h_q, n_hg, topk, xtopk, Tm, T;
+  int64_t pool_tokens, xpool_tokens;
+  float scale_log2;         // sm_scale * log2(e)
+};
+
+// Work plan derived from the problem shape and the SM count.
+struct Plan {
+  int nh;          // heads per CTA (16, 32 or 64)
+  int n_hg;        // head groups = h_q / nh
+  int Tm, Te, T;   // tiles per query token: main, extra, total
+  int64_t G;       // total (query token, tile) items
+  int64_t S;       // items per part
+  int num_parts;
+  int64_t max_splits;
+  size_t ws_o_bytes, ws_bytes;
+};
+
+template <int NH>
+cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
+int decode_smem_bytes(int nh);
+
+cudaError_t launch_metadata(const Plan& plan, int nq, int32_t* d_sched, int32_t* d_num_splits, cudaStream_t stream);
+
+cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, const float* lse_part, uint16_t* out,
+                           float* lse, int nq, int h_q, bool skip_single, cudaStream_t stream);
+
+cudaError_t launch_dequant(int kv_format, const uint8_t* records, int64_t n, uint16_t* out, cudaStream_t stream);
+
+}  // namespace mla

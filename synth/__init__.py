@@ -328,12 +328,14 @@ def compact(w: Workload, queries) -> dict:
     out = dict(q_bits=q)
 
     def remap(ids, pos, rec):
-        valid = ids >= 0
-        loc = np.searchsorted(pos, ids[valid])
-        assert np.all(pos[loc] == ids[valid])
-        uniq, inv = np.unique(loc, return_inverse=True)
-        new = np.full(ids.shape, -1, dtype=np.int32)
-        new[valid] = inv.astype(np.int32)
+        # Entries that name no generated record (outside the contract) become
+        # -2, which a reference skips just as it skips out-of-range entries.
+        loc = np.searchsorted(pos, np.where(ids >= 0, ids, 0))
+        loc = np.minimum(loc, max(pos.shape[0] - 1, 0))
+        known = (ids >= 0) & (pos.shape[0] > 0) & (pos[loc] == ids)
+        uniq, inv = np.unique(loc[known], return_inverse=True)
+        new = np.where(ids == -1, -1, -2).astype(np.int32)
+        new[known] = inv.astype(np.int32)
         return new, rec[uniq]
 
     out["idx"], out["kv"] = remap(ids, w.ref_pos, w.ref_rec)

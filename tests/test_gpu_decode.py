@@ -1,0 +1,178 @@
+"""GPU decode parity against the fp64 oracle, element by element.
+
+Tolerances: |out - ref| <= 1e-2 + 1e-2 |ref| (bf16 outputs), |lse - ref| <=
+1e-3 (natural log).  Every pool is filled with a poison byte wherever no
+index points, so a read of an unselected record would show in the output.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_kv_cache_sparse_gb300 as mla
+import oracle
+import synth
+from _harness import DeviceWorkload, all_queries, compare, sample_queries
+
+pytestmark = pytest.mark.gpu
+
+REDUCED_BATCH = {0: 1, 1: 4, 2: 2, 3: 4, 4: 1, 5: 3}
+
+
+@pytest.mark.parametrize("cid", [0, 1, 2, 3, 4, 5])
+def test_reduced_configs_all_queries(cid):
+    """Every query token of each workload family at a batch the oracle
+    finishes in seconds (several tiles per query, ragged -1 tails)."""
+    w = synth.make_workload(cid, batch=REDUCED_BATCH[cid], workers=1)
+    dw = DeviceWorkload(w)
+    out, lse, err = dw.run()
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_full_size_sampled_queries(cid):
+    """The full workload in the launch configuration the benchmark times;
+    sampled query tokens against the oracle, the rest checked for finiteness
+    and the -inf/0 convention."""
+    w = synth.make_workload(cid)
+    dw = DeviceWorkload(w)
+    out, lse, err = dw.run()
+    assert err == 0
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    compare(out, lse, w, sample_queries(w, n=3, seed=cid))
+
+
+def test_scattered_skips():
+    for cid in (1, 2):
+        w = synth.make_workload(cid, batch=2, scattered_neg=True, workers=1)
+        out, lse, err = DeviceWorkload(w).run()
+        compare(out, lse, w, all_queries(w))
+
+
+def _custom(h_q, topk, pool, idx, q_scale=1.0, seed=0, xpool=0, xidx=None, s=1):
+    """A workload from explicit index arrays (idx int [b, s, topk])."""
+    rng = np.random.default_rng(seed)
+    b = idx.shape[0]
+    cfg = synth.Config(99, "custom", b, s, h_q, pool, topk,
+                       extra_pool=xpool, extra_topk=0 if xidx is None else xidx.shape[-1])
+    q = (rng.standard_normal((b, s, h_q, 512), dtype=np.float32) * q_scale).astype(np.float32)
+    pos = np.unique(idx[(idx >= 0) & (idx < pool * b)])
+    rec = synth.encode_fp8_records(rng.standard_normal((pos.shape[0], 512), dtype=np.float32))
+    w = synth.Workload(cfg=cfg, q_bits=synth.f32_to_bf16_bits(q), idx=idx.astype(np.int32),
+                       pool_tokens=pool * b, ref_pos=pos.astype(np.int64), ref_rec=rec)
+    if xidx is not None:
+        xpos = np.unique(xidx[xidx >= 0])
+        w.extra_idx = xidx.astype(np.int32)
+        w.extra_pool_tokens = xpool * b
+        w.extra_ref_pos = xpos.astype(np.int64)
+        w.extra_ref_rec = synth.encode_fp4_records(rng.standard_normal((xpos.shape[0], 512), dtype=np.float32))
+    return w
+
+
+def _random_idx(rng, b, s, topk, pool, neg=0.0):
+    idx = np.stack([np.stack([bi * pool + rng.choice(pool, topk, replace=False) for _ in range(s)])
+                    for bi in range(b)])
+    if neg:
+        idx[rng.random(idx.shape) < neg] = -1
+    return idx
+
+
+@pytest.mark.parametrize("h_q", [16, 32, 64, 128])
+@pytest.mark.parametrize("topk", [1, 127, 129, 300])
+def test_heads_and_ragged_topk(h_q, topk):
+    rng = np.random.default_rng(h_q * 1000 + topk)
+    idx = _random_idx(rng, 3, 1, topk, 512, neg=0.1)
+    w = _custom(h_q, topk, 512, idx, seed=topk)
+    out, lse, err = DeviceWorkload(w).run()
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
+def test_all_skipped_rows_give_zero_and_neg_inf():
+    rng = np.random.default_rng(7)
+    idx = _random_idx(rng, 4, 1, 200, 256)
+    idx[1] = -1
+    idx[3, 0, :130] = -1          # first tile empty, second partly valid
+    w = _custom(64, 200, 256, idx)
+    out, lse, err = DeviceWorkload(w).run()
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    assert not torch.signbit(out[1].float()).any()
+    compare(out, lse, w, all_queries(w))
+
+
+def test_extra_cache_joint_softmax_and_extra_only_rows():
+    rng = np.random.default_rng(8)
+    idx = _random_idx(rng, 3, 1, 256, 512, neg=0.05)
+    xidx = _random_idx(rng, 3, 1, 130, 192, neg=0.05)
+    idx[2] = -1                    # this row is attended through the extra cache alone
+    w = _custom(64, 256, 512, idx, xpool=192, xidx=xidx)
+    out, lse, err = DeviceWorkload(w).run()
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
+def test_duplicate_indices_count_twice():
+    rng = np.random.default_rng(9)
+    idx = _random_idx(rng, 2, 1, 100, 320)
+    idx[:, :, 50:] = idx[:, :, :50]
+    w = _custom(16, 100, 320, idx)
+    out, lse, _ = DeviceWorkload(w).run()
+    compare(out, lse, w, all_queries(w))
+
+
+def test_bad_indices_are_skipped_and_flagged():
+    rng = np.random.default_rng(10)
+    idx = _random_idx(rng, 2, 1, 150, 448)
+    idx[0, 0, 5] = 2 * 448 + 7       # past the pool (7 pages per sequence)
+    idx[1, 0, 140] = -5              # negative, not -1
+    w = _custom(32, 150, 448, idx)
+    out, lse, err = DeviceWorkload(w).run()
+    assert err & mla.DEVERR_BAD_INDEX
+    compare(out, lse, w, all_queries(w))
+
+
+def test_large_scores_exercise_rescaling():
+    """Scores spread over many units: the running max moves by more than the
+    lazy-rescale threshold inside a query token."""
+    rng = np.random.default_rng(11)
+    idx = _random_idx(rng, 3, 2, 1024, 2048)
+    w = _custom(64, 1024, 2048, idx, q_scale=6.0, s=2)
+    out, lse, _ = DeviceWorkload(w).run()
+    compare(out, lse, w, all_queries(w))
+
+
+@pytest.mark.parametrize("num_sms", [1, 3, 152, 100000])
+def test_split_counts_do_not_change_results(num_sms):
+    """From one part (no split) to one tile per part (every query split into
+    all its tiles)."""
+    w = synth.make_workload(1, batch=3, workers=1)
+    dw = DeviceWorkload(w)
+    out, lse, err = dw.run(num_sms=num_sms)
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
+def test_deterministic():
+    w = synth.make_workload(2, batch=2, workers=1)
+    dw = DeviceWorkload(w)
+    dec = dw.decoder()
+    o1, l1, _ = dw.run(dec=dec)
+    o1, l1 = o1.clone(), l1.clone()
+    o2, l2, _ = dw.run(dec=dec)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+def test_topk1_returns_the_latent():
+    rng = np.random.default_rng(12)
+    idx = _random_idx(rng, 2, 1, 1, 64)
+    w = _custom(16, 1, 64, idx)
+    out, lse, _ = DeviceWorkload(w).run()
+    for b in range(2):
+        g = np.searchsorted(w.ref_pos, idx[b, 0, 0])
+        k = oracle.bf16_rne(oracle.dequant_fp8(w.ref_rec[g:g + 1]))[0]
+        got = out[b, 0].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.all(got == k[None, :])
+    compare(out, lse, w, all_queries(w))
