@@ -1,0 +1,393 @@
+"""Benchmark of token-sparse MLA decode on GB300 (one JSON line on stdout).
+
+Headline workload: batch 128, seq_len_q 2, h_q 128, topk 2048 (half from the
+last 4096 positions), 131072-token FP8 pool per sequence -- the heavy-heads
+decode step on which the >= 60 %-of-roofline target is set.  A step is one
+mla_sparse_decode call (decode kernel + split merge) over the whole batch,
+inputs resident in HBM; L2 is flushed (512 MB write) between timed steps,
+outside the timed events.  The other workloads are reported under
+"per_config".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm: a slow,
+obviously correct restatement) on bounded samples of the same workload.
+Under torchrun every rank decodes its own replica of the workload on its
+own GPU (weak scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "sparse MLA decode TFLOP/s and KV GB/s on 1 GB300; fraction of roofline"
+HEADLINE = 2
+SECONDARY = [0, 1, 3, 4, 5]
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["fp4_kv_cache_sparse_gb300/csrc/decode.cu", "fp4_kv_cache_sparse_gb300/csrc/mla_device.cuh"]
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampling in the background; summarised over a time window."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.rows = []
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(row[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + row[0].strip().split(".")[1]) if "." in row[0] else 0.0
+                self.rows.append(dict(t=ts + frac, sm=float(row[2]), sm_max=float(row[3]),
+                                      reasons=[k for k, v in zip(
+                                          ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                           "sw_power_cap"], row[6:10]) if v.strip() == "Active"]))
+            except (ValueError, IndexError):
+                continue
+
+    def summary(self, t_begin: float, t_end: float):
+        rows = [r for r in self.rows if t_begin - 0.06 <= r["t"] <= t_end + 0.06]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({x for r in rows for x in r["reasons"]})
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def roofline_of(flops, kv_bytes, seconds, pk):
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = kv_bytes / (pk["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    return bound, max(t_tc, t_hbm) / seconds
+
+
+def build_device(w, dev):
+    """Device copies of a workload (pools poisoned where unreferenced) and a
+    decoder planned for its shape."""
+    import fp4_kv_cache_sparse_gb300 as mla
+
+    class DW:
+        pass
+
+    def pool(pos, rec, tokens):
+        t = torch.full((tokens, rec.shape[1]), synth.POISON_BYTE, dtype=torch.uint8, device=dev)
+        t[torch.from_numpy(pos).to(dev)] = torch.from_numpy(rec).to(dev)
+        return t
+
+    dw = DW()
+    dw.q = torch.from_numpy(w.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    dw.idx = torch.from_numpy(w.idx).to(dev)
+    dw.kv = pool(w.ref_pos, w.ref_rec, w.pool_tokens)
+    dw.xkv = dw.xidx = None
+    if w.extra_idx is not None:
+        dw.xkv = pool(w.extra_ref_pos, w.extra_ref_rec, w.extra_pool_tokens)
+        dw.xidx = torch.from_numpy(w.extra_idx).to(dev)
+    c = w.cfg
+    problem = mla.Problem.make(c.batch, c.seq_len_q, c.h_q, c.topk, w.pool_tokens // 64,
+                               extra_topk=c.extra_topk, extra_num_pages=w.extra_pool_tokens // 64,
+                               sm_scale=float(w.sm_scale))
+    return dw, mla.SparseMLADecoder(problem, dev)
+
+
+def time_decode(dw, dec, steps, warmup, flush, dev_barrier=None):
+    """Per-step CUDA-event durations of the decode call, L2 flushed between."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        dec(dw.q, dw.kv, dw.idx, dw.xkv, dw.xidx)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if dev_barrier:
+        dev_barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        dec(dw.q, dw.kv, dw.idx, dw.xkv, dw.xidx)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dev_barrier:
+        dev_barrier()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return ms, t0, t1
+
+
+def time_e2e(dw, dec, steps, warmup):
+    """Through the public API with HOST buffers: pinned q and indices copied
+    in, the decode, the output and LSE copied back, every step."""
+    q_h = dw.q.cpu().pin_memory()
+    idx_h = dw.idx.cpu().pin_memory()
+    xidx_h = dw.xidx.cpu().pin_memory() if dw.xidx is not None else None
+    out_h = torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(tuple(dw.q.shape[:3]), dtype=torch.float32).pin_memory()
+    q_d, idx_d = torch.empty_like(dw.q), torch.empty_like(dw.idx)
+    xidx_d = torch.empty_like(dw.xidx) if dw.xidx is not None else None
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        idx_d.copy_(idx_h, non_blocking=True)
+        if xidx_d is not None:
+            xidx_d.copy_(xidx_h, non_blocking=True)
+        out, lse = dec(q_d, dw.kv, idx_d, dw.xkv, xidx_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    h2d = q_h.numel() * 2 + idx_h.numel() * 4 + (xidx_h.numel() * 4 if xidx_h is not None else 0)
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return dt, h2d, d2h
+
+
+def oracle_rate(w, budget_s=12.0, max_queries=None):
+    """The oracle as it stands on a bounded sample of query tokens of w:
+    returns (TFLOP/s, sample description, seconds, threads)."""
+    import oracle
+    qs = [(b, s) for b in range(w.cfg.batch) for s in range(w.cfg.seq_len_q)]
+    n = 1
+    done_flops, done_s, used = 0.0, 0.0, 0
+    order = np.random.default_rng(0).permutation(len(qs))
+    while used < len(qs) and done_s < budget_s and (max_queries is None or used < max_queries):
+        pick = [qs[i] for i in order[used:used + n]]
+        c = synth.compact(w, pick)
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(c["q_bits"], c["kv"], c["idx"], w.sm_scale,
+                                 extra_kv=c.get("extra_kv"), extra_idx=c.get("extra_idx"))
+        done_s += time.perf_counter() - t0
+        valid = (c["idx"] >= 0).sum() + ((c["extra_idx"] >= 0).sum() if "extra_idx" in c else 0)
+        done_flops += 4.0 * 512 * w.cfg.h_q * float(valid)
+        used += len(pick)
+        n = min(2 * n, 64)
+    desc = f"{used} of {len(qs)} query tokens of {w.cfg.name}, oracle on compacted pools"
+    return done_flops / done_s / 1e12, desc, done_s, oracle.num_threads()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = synth.make_workload(HEADLINE)
+    cfg = w.cfg
+    qs = [(b, s) for b in range(cfg.batch) for s in range(cfg.seq_len_q)]
+    rng = np.random.default_rng(1)
+
+    def one_step():
+        pick = [qs[i] for i in rng.choice(len(qs), 2, replace=False)]
+        c = synth.compact(w, pick)
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(c["q_bits"], c["kv"], c["idx"], w.sm_scale)
+        dt = time.perf_counter() - t0
+        return 4.0 * 512 * cfg.h_q * float((c["idx"] >= 0).sum()), dt
+
+    for _ in range(args.warmup):
+        one_step()
+    fl, sec = 0.0, 0.0
+    for _ in range(args.steps):
+        f, d = one_step()
+        fl += f
+        sec += d
+    value = fl / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "seq_len_q": cfg.seq_len_q, "h_q": cfg.h_q,
+                   "topk": cfg.topk, "pool_per_seq": cfg.pool,
+                   "step": "fp64 oracle on 2 random query tokens of the workload (compacted pools)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} steps x 2 query tokens of {cfg.name}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    clocks = Clocks(local) if rank == 0 else None
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        barrier = lambda: dist.barrier(device_ids=[local])  # noqa: E731
+
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    w = synth.make_workload(HEADLINE, seed=synth.SEED_BASE + HEADLINE + 7919 * rank)
+    flops, kvb = synth.flops(w), synth.kv_bytes(w)
+    dw, dec = build_device(w, dev)
+    dec_parts = dec.num_parts
+    ms, t0, t1 = time_decode(dw, dec, args.steps, args.warmup, flush, barrier)
+    step_s = statistics.mean(ms) * 1e-3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_s = float(t.item())
+    value = world * flops / step_s / 1e12
+    e2e_s, h2d, d2h = time_e2e(dw, dec, max(20, args.steps // 20), args.warmup)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    bound, frac = roofline_of(flops, kvb, step_s, pk)
+    per_rank_achieved = flops / step_s / 1e12 if bound == "tensor" else kvb / step_s / 1e9
+    traffic = profiled_traffic(w.cfg.name)
+
+    per_config = {}
+    if not args.no_secondary:
+        del dw, dec
+        torch.cuda.empty_cache()
+        for cid in SECONDARY:
+            wc = synth.make_workload(cid, seed=synth.SEED_BASE + cid + 7919 * rank)
+            f2, b2 = synth.flops(wc), synth.kv_bytes(wc)
+            dwc, decc = build_device(wc, dev)
+            msc, _, _ = time_decode(dwc, decc, max(50, args.steps // 10), args.warmup, flush, barrier)
+            sc = statistics.mean(msc) * 1e-3
+            bnd, fr = roofline_of(f2, b2, sc, pk)
+            per_config[wc.cfg.name] = {"us": round(sc * 1e6, 2), "tflops": round(f2 / sc / 1e12, 2),
+                                       "kv_gbs": round(b2 / sc / 1e9, 1), "bound": bnd,
+                                       "roofline_frac": round(fr, 4), "flops": f2, "kv_bytes": b2}
+            del dwc, decc
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc, secs, cores = oracle_rate(w)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": round(secs, 2)}
+    if clocks:
+        clocks.stop()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.cfg.name, "batch": w.cfg.batch, "seq_len_q": w.cfg.seq_len_q,
+                   "h_q": w.cfg.h_q, "head_dim": 512, "topk": w.cfg.topk, "pool_per_seq": w.cfg.pool,
+                   "kv_format": "fp8_528", "l2": "flushed between steps (512 MB write, outside the timed events)",
+                   "step": "mla_sparse_decode: decode kernel + split merge", "parallelism": f"replicas x{world}"},
+        "kv_gbs": world * kvb / step_s / 1e9,
+        "roofline": {"bound": bound, "achieved": per_rank_achieved,
+                     "peak": pk["bf16_tflops"] if bound == "tensor" else pk["hbm_gbs"],
+                     "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                     "frac": frac, "traffic": traffic, "peak_source": pk["source"] + " (burst)",
+                     "kernel": "decode kernel + split merge, CUDA events around the mla_sparse_decode call"},
+        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": (2 if dec_parts > 1 else 1) * args.steps,
+        "clocks": clocks.summary(t0, t1) if clocks else None,
+        "cpu_baseline": cpu,
+        "per_config": per_config,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
