@@ -298,6 +298,10 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default=str(HEADLINE), help="workload id or name for the headline line")
+    ap.add_argument("--batch", type=int, default=None, help="override the number of sequences")
+    ap.add_argument("--pool", type=int, default=None, help="override the tokens per sequence")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
@@ -317,7 +321,8 @@ def main():
         barrier = lambda: dist.barrier(device_ids=[local])  # noqa: E731
 
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
-    w = synth.make_workload(HEADLINE, seed=synth.SEED_BASE + HEADLINE + 7919 * rank)
+    wid = int(args.workload) if args.workload.isdigit() else synth.BY_NAME[args.workload].id
+    w = synth.make_workload(wid, seed=synth.SEED_BASE + wid + 7919 * rank, batch=args.batch, pool=args.pool)
     flops, kvb = synth.flops(w), synth.kv_bytes(w)
     dw, dec = build_device(w, dev)
     dec_parts = dec.num_parts
@@ -329,7 +334,8 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         step_s = float(t.item())
     value = world * flops / step_s / 1e12
-    e2e_s, h2d, d2h = time_e2e(dw, dec, max(20, args.steps // 20), args.warmup)
+    e2e_s, h2d, d2h = (float("nan"), 0, 0) if args.no_e2e else time_e2e(dw, dec, max(20, args.steps // 20),
+                                                                          args.warmup)
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([e2e_s], device=dev)
@@ -369,7 +375,8 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.cfg.name, "batch": w.cfg.batch, "seq_len_q": w.cfg.seq_len_q,
+        "config": {"workload": w.cfg.name + ("" if (args.batch, args.pool) == (None, None) else " (resized)"),
+                   "batch": w.cfg.batch, "seq_len_q": w.cfg.seq_len_q,
                    "h_q": w.cfg.h_q, "head_dim": 512, "topk": w.cfg.topk, "pool_per_seq": w.cfg.pool,
                    "kv_format": "fp8_528", "l2": "flushed between steps (512 MB write, outside the timed events)",
                    "step": "mla_sparse_decode: decode kernel + split merge", "parallelism": f"replicas x{world}"},

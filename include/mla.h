@@ -184,6 +184,32 @@ mla_status_t mla_combine(const mla_problem_t* problem, const int32_t* d_num_spli
 mla_status_t mla_dequantize(int32_t kv_format, const void* records, int64_t n, void* out,
                             mla_stream_t stream);
 
+/*
+ * Decode without a caller-provided workspace.  The pages have no counterpart
+ * to this entry point; it exists for callers that may not allocate device
+ * memory at call time -- a plugin or hook inside another runtime that hands
+ * it only input and output buffers, or a serving loop whose device memory is
+ * all reserved up front by its own pool and which may not call cudaMalloc on
+ * its per-step path.
+ *
+ * Same arguments and result as mla_sparse_decode minus the workspace: the
+ * split partials go to a fixed array of MLA_NOALLOC_SCRATCH_BYTES that every
+ * device loading this library holds until the process exits.  The first call
+ * on a device looks up that array's device address (make it before any stream
+ * capture).  Returns MLA_ERR_WORKSPACE, with nothing enqueued, when the
+ * problem's workspace (the bytes mla_get_metadata reports for it) exceeds
+ * MLA_NOALLOC_SCRATCH_BYTES.  All calls share the one array: calls that
+ * overlap on the GPU race and must be serialised by the caller (one stream).
+ * Allocates nothing.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
+mla_status_t mla_sparse_decode_noalloc(const mla_problem_t* problem,
+                                       const void* q, const void* kv, const int32_t* indices,
+                                       const void* extra_kv, const int32_t* extra_indices,
+                                       const int32_t* d_sched, const int32_t* d_num_splits, int32_t num_parts,
+                                       void* out, float* lse, int32_t* d_error,
+                                       mla_stream_t stream);
+
 /* Static description of a status code. */
 const char* mla_status_string(mla_status_t status);
 

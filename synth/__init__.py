@@ -251,19 +251,22 @@ def _encode_chunks(base_seed: int, kind: int, n: int, workers: Optional[int]) ->
 
 def make_workload(cfg: Config | int | str, seed: Optional[int] = None,
                   scattered_neg: bool = False, batch: Optional[int] = None,
-                  workers: Optional[int] = None) -> Workload:
+                  workers: Optional[int] = None, pool: Optional[int] = None) -> Workload:
     """Draw the workload of a configuration.
 
     scattered_neg moves the -1 entries of a 'trailing' configuration to random
-    slots.  batch < cfg.batch draws only the first sequences (same values as
-    the full draw is NOT promised; it is a smaller workload of the same
-    shape family)."""
+    slots.  batch / pool override the number of sequences and the tokens per
+    sequence: a smaller workload of the same family (its values are not a
+    subset of the full draw)."""
     if isinstance(cfg, int):
         cfg = CONFIGS[cfg]
     elif isinstance(cfg, str):
         cfg = BY_NAME[cfg]
     if batch is not None and batch != cfg.batch:
         cfg = dataclasses.replace(cfg, batch=batch)
+    if pool is not None and pool != cfg.pool:
+        assert pool % PAGE_SIZE == 0 and pool >= cfg.topk and pool > cfg.recent_window
+        cfg = dataclasses.replace(cfg, pool=pool)
     if scattered_neg:
         cfg = dataclasses.replace(cfg, neg_mode="random")
     base_seed = SEED_BASE + cfg.id if seed is None else seed
