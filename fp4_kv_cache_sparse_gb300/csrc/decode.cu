@@ -1,4 +1,4 @@
-// decode.cu -- token-sparse MLA decode kernel for sm_103a (tcgen05 + TMEM).
+// decode.cu -- token-sparse MLA decode kernel for sm_103a (tcgen05 + TMEM + TMA).
 //
 // What it computes ("flops/flashmla-decode-fp8-fp4-kv", sections "Arithmetic
 // intensity" and "Workarounds"; "deepseek-ai/FlashMLA", "How to use it"):
@@ -7,25 +7,33 @@
 // cache) or FP4 (extra cache) record and used as both key and value, one
 // online softmax over all selected tokens, output plus log-sum-exp.
 //
-// Structure of one CTA (288 threads), which owns one head group (NH heads)
-// of a contiguous run of (query token, tile) work items:
-//   warps 4-7  producers: gather the 128 records of a tile with 16-byte
-//              read-only loads, dequantize in registers (exact, bf16), write
-//              the bf16 tile into shared memory in the 128-byte-swizzled
-//              canonical layout, one 128-dim quarter at a time.
-//   warp 8     tensor-core issuer: S^T = K Q^T (M = 128 tokens, N = NH heads,
-//              K = 512) into TMEM, then O^T += V^T P^T (M = 128 dims per
-//              quarter, N = NH, K = 128 tokens).  The same shared tile is the
-//              K-major A operand of the first product and the MN-major A
-//              operand of the second (K = V = the latent).
-//   warps 0-3  softmax: thread i owns TMEM lane i (token i of the tile):
-//              scale, mask, column max and sum over the 128 tokens
-//              (shuffle reduce-scatter + shared memory), lazy rescale of O,
-//              P^T to shared memory; at the end of a query token, normalise
-//              O^T and write the output (or a split partial) and the LSE.
-// Hand-offs use mbarriers; tensor-core completion is signalled with
-// tcgen05.commit.  Every wait is bounded (see mbar_wait).
+// One CTA (384 threads, one per SM) owns one head group (NH heads) of a
+// contiguous run of (query token, 128-slot tile) work items:
+//   warps 4-11  producers.  Each warp owns 16 token rows of a tile.  Record
+//               bytes are loaded with 16-byte read-only loads one whole tile
+//               ahead (registers), indices two tiles ahead; a quarter (128
+//               dims) is dequantized exactly to bf16 in registers and stored
+//               into shared memory in the 128-byte-swizzled canonical layout
+//               as soon as the tensor core has released that quarter.
+//               Lane 0 of warp 4 also fetches each query token's Q by TMA.
+//   warps 0-3   softmax; thread 0 also issues the tensor-core work:
+//               S^T = K Q^T (M = 128 tokens, N = NH heads, K = 512) into TMEM
+//               quarter by quarter as the producers deliver them, then
+//               O^T += V^T P^T (M = 128 dims per quarter, N = NH, K = 128
+//               tokens).  The same shared tile is the K-major A operand of
+//               the first product and the MN-major A operand of the second.
+//               Thread i owns TMEM lane i (token i): it scales and masks its
+//               row of S^T and checks it against the running per-head maxima;
+//               only when some score exceeds its head's maximum by more than
+//               2^8 are exact column maxima computed (shuffle reduce-scatter)
+//               and O^T, l rescaled.  P^T goes to shared memory; each thread's
+//               running row sums live in spare TMEM columns of its own lane
+//               until the end of the query token.
+// Hand-offs use mbarriers (tensor-core completion via tcgen05.commit, TMA
+// completion via transaction counts) and one named barrier inside the
+// softmax warps.  Every mbarrier wait is bounded (see mbar_wait).
 #include <cstdint>
+#include <cuda.h>
 
 #include "mla_device.cuh"
 #include "mla_internal.h"
@@ -34,14 +42,16 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;
-constexpr int kProducerBase = 128;
-constexpr int kMmaWarp = 8;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr int kProducerWarps = 8;
+constexpr int kRowsPerProducerWarp = kTile / kProducerWarps;  // 16
+constexpr int kRounds = kRowsPerProducerWarp / 4;              // 4 loads of 4 tokens x 8 lanes
+constexpr uint64_t kWaitLimitNs = 2000000000ull;               // 2 s per wait
 
-// Softmax stays exact with a stale running max as long as the scores it
-// subtracts from stay within 2^kLazy of it.
+// Scores may exceed the running maximum they are exponentiated against by
+// up to 2^kLazy before the maximum is moved (P <= 2^8 stays exact enough in
+// bf16 and the fp32 sums cannot overflow).
 constexpr float kLazyRescale = 8.0f;
 
 template <int NH>
@@ -53,8 +63,7 @@ struct Smem {
   static constexpr int kQOff = kKvOff + kKvBytes;
   static constexpr int kPOff = kQOff + kQBytes;
   static constexpr int kMiscOff = kPOff + kPBytes;
-  // misc: 16 mbarriers, then scalars, then per-head arrays
-  static constexpr int kBarOff = kMiscOff;
+  static constexpr int kBarOff = kMiscOff;              // 16 mbarriers
   static constexpr int kScalarOff = kBarOff + 16 * 8;
   static constexpr int kRedOff = kScalarOff + 64;       // float[4][NH]
   static constexpr int kMOff = kRedOff + 4 * NH * 4;    // float[NH]
@@ -65,12 +74,12 @@ struct Smem {
   static constexpr uint32_t kTmemCols = NH == 64 ? 512 : (NH == 32 ? 256 : 128);
 };
 
-enum Bar { kQuarterFull = 0, kQuarterFree = 4, kSFull = 8, kPFull, kOReady, kQFull, kQFree, kDrain };
+enum Bar { kQuarterFull = 0, kQuarterFree = 4, kSFull = 8, kOReady, kQFull, kQFree, kDrain };
 
 // Reduce-scatter of v[N] over the 32 lanes of a warp.  Afterwards lane l
 // holds in v[0 .. max(N/32,1)) the reduction over all lanes of heads
-// head_of(l, k) (see below).  Each step halves the values a lane keeps and
-// exchanges the other half with the partner lane.
+// rs_head<N>(l, k).  Each step halves the values a lane keeps and exchanges
+// the other half with the partner lane.
 template <int SIZE, int O>
 struct ReduceScatter {
   template <int N, typename Op>
@@ -113,6 +122,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_stream8(const uint8_t* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// TMA: arm an mbarrier with the bytes it will receive; 2-D tiled load.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Work decomposition shared by all roles of a CTA.
@@ -161,8 +209,59 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int qidx, i
   return ti;
 }
 
+// One producer lane's view of a tile: its 4 token slots (one per load
+// round), each -1 when there is nothing to load.
+struct LaneTile {
+  int32_t id[kRounds];
+  bool extra;
+};
+
+__device__ __forceinline__ LaneTile lane_tile(const DecodeParams& p, int64_t g, int row0, bool flag_bad) {
+  LaneTile lt;
+  const int qidx = static_cast<int>(g / p.T);
+  const TileInfo ti = tile_info(p, qidx, static_cast<int>(g - static_cast<int64_t>(qidx) * p.T));
+  lt.extra = ti.extra;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int slot = ti.slot0 + row0 + r * 4;
+    const int32_t id = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
+    const bool valid = id >= 0 && static_cast<int64_t>(id) < ti.pool;
+    if (!valid && id != -1 && flag_bad && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_INDEX);
+    lt.id[r] = valid ? id : -1;
+  }
+  return lt;
+}
+
+// Register-resident bytes of one quarter (128 dims) of the lane's 4 tokens.
+struct QuarterRegs {
+  uint4 data[kRounds];   // FP8: 16 e4m3 bytes; FP4: .x/.y = 8 bytes of e2m1 pairs
+  uint32_t scale[kRounds];
+};
+
+__device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTile& lt, int qq, int s8,
+                                             QuarterRegs& q) {
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int32_t id = lt.id[r];
+    if (id < 0) {
+      q.data[r] = make_uint4(0, 0, 0, 0);
+      q.scale[r] = lt.extra ? 0x38u : 127u * 0x01010101u;
+    } else if (!lt.extra) {
+      const uint8_t* rec = p.kv + static_cast<int64_t>(id) * kRecFp8;
+      q.data[r] = ldg_stream16(rec + qq * 128 + s8 * 16);
+      q.scale[r] = ldg_u32(rec + 512 + qq * 4);
+    } else {
+      const uint8_t* rec = p.xkv + static_cast<int64_t>(id) * kRecFp4;
+      const uint2 d = ldg_stream8(rec + qq * 64 + s8 * 8);
+      q.data[r] = make_uint4(d.x, d.y, 0, 0);
+      q.scale[r] = ldg_u8(rec + 256 + qq * 8 + s8);
+    }
+  }
+}
+
 template <int NH>
-__global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap q_map) {
   using L = Smem<NH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -185,20 +284,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
 
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars[kQuarterFull + i], 4);
+      mbar_init(&bars[kQuarterFull + i], kProducerWarps);
       mbar_init(&bars[kQuarterFree + i], 1);
     }
     mbar_init(&bars[kSFull], 1);
-    mbar_init(&bars[kPFull], kSoftmaxThreads);
     mbar_init(&bars[kOReady], 1);
-    mbar_init(&bars[kQFull], 4);
+    mbar_init(&bars[kQFull], 1);
     mbar_init(&bars[kQFree], 1);
     mbar_init(&bars[kDrain], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, L::kTmemCols);
+  if (tid < NH) sm_m[tid] = -INFINITY;
+  if (warp == 1) tmem_alloc(tmem_slot, L::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -207,133 +306,139 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
   const Span span = load_span(p, part);
   if (!span.ok && tid == 0 && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_METADATA);
 
-  if (warp >= 4 && warp < 8) {
+  if (warp >= 4) {
     // ------------------------------------------------------------------
-    // Producers: Q of each query token, then the dequantized tiles.
+    // Producers.
     // ------------------------------------------------------------------
-    const int pt = tid - kProducerBase;
-    const int pw = pt >> 5;
-    const int j4 = lane >> 3;  // token of the 4 a load instruction covers
-    const int s8 = lane & 7;   // 16-value segment within a 128-dim quarter
+    const int pw = warp - 4;
+    const int j4 = lane >> 3;  // token of the 4 one load instruction covers
+    const int s8 = lane & 7;   // 16-dim segment within a 128-dim quarter
+    const int row0 = pw * kRowsPerProducerWarp + j4;
+    const bool flag_bad = hg == 0 && s8 == 0;
+    // Store geometry: chunk 2qq + s8/4, 16-byte units 2(s8&3), +1; lanes
+    // 4-7 of a quarter-warp store the odd unit first so the 8 lanes of a
+    // store phase hit 8 different bank groups.
+    const uint32_t u0 = 2 * (s8 & 3);
+    const bool swap = (s8 & 4) != 0;
+
     uint32_t n_tile = 0, n_seg = 0;
-    for (int64_t g = span.g_begin; g < span.g_end;) {
-      const int qidx = static_cast<int>(g / p.T);
-      const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-      // Q (NH heads of this head group), K-major, 128-byte swizzle.
-      if (n_seg > 0) mbar_wait(&bars[kQFree], (n_seg - 1) & 1, abort_flag, p.d_error, kWaitLimitNs);
-      {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<int64_t>(qidx) * p.h_q + static_cast<int64_t>(hg) * NH) * kD);
-#pragma unroll 4
-        for (int u = pt; u < NH * 64; u += 128) {
-          const int h = u >> 6, d8 = u & 63;
-          const uint4 v = __ldg(qsrc + u);
-          const uint32_t off = (d8 >> 3) * (NH * 128) + swz<128>(h * 128 + (d8 & 7) * 16);
-          *reinterpret_cast<uint4*>(sQ + off) = v;
+    int64_t g = span.g_begin;
+    LaneTile cur{}, nxt{};
+    QuarterRegs buf[4];
+    if (g < span.g_end) {
+      cur = lane_tile(p, g, row0, flag_bad);
+      if (g + 1 < span.g_end) nxt = lane_tile(p, g + 1, row0, flag_bad);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) load_quarter(p, cur, qq, s8, buf[qq]);
+    }
+    int64_t seg_end = g;  // forces a segment start on the first tile
+    for (; g < span.g_end; ++g, ++n_tile) {
+      if (g == seg_end) {
+        // First tile of a query token: its Q by TMA once the previous
+        // token's last S^T no longer reads shared Q.
+        const int qidx = static_cast<int>(g / p.T);
+        seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
+        if (pw == 0 && lane == 0) {
+          if (n_seg > 0) mbar_wait(&bars[kQFree], (n_seg - 1) & 1, abort_flag, p.d_error, kWaitLimitNs);
+          mbar_expect_tx(&bars[kQFull], NH * kD * 2);
+          const int y = qidx * p.h_q + hg * NH;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) tma_load_2d(sQ + c * (NH * 128), &q_map, c * 64, y, &bars[kQFull]);
+        }
+        ++n_seg;
+      }
+      const bool extra = cur.extra;
+      LaneTile nxt2{};
+      if (g + 2 < span.g_end) nxt2 = lane_tile(p, g + 2, row0, flag_bad);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        if (n_tile > 0) mbar_wait(&bars[kQuarterFree + qq], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitLimitNs);
+        uint8_t* chunk = sKV + (2 * qq + (s8 >> 2)) * 16384;
+        if (!extra) {
+          uint32_t sb[kRounds];
+#pragma unroll
+          for (int r = 0; r < kRounds; ++r) sb[r] = (buf[qq].scale[r] >> (8 * (s8 >> 1))) & 0xFFu;
+          bool any_big = false;
+#pragma unroll
+          for (int r = 0; r < kRounds; ++r) any_big |= sb[r] > 142u;
+          any_big = __any_sync(0xFFFFFFFFu, any_big);
+#pragma unroll
+          for (int r = 0; r < kRounds; ++r) {
+            uint32_t o[8];
+            if (!any_big)
+              dequant_fp8_16_small_scale(buf[qq].data[r], sb[r], o);
+            else
+              dequant_fp8_16(buf[qq].data[r], sb[r], o);
+            const uint32_t row = row0 + r * 4;
+            const uint32_t oa = swz<128>(row * 128 + u0 * 16);
+            const uint32_t ob = swz<128>(row * 128 + (u0 + 1) * 16);
+            const uint4 a = make_uint4(o[0], o[1], o[2], o[3]);
+            const uint4 b = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(chunk + (swap ? ob : oa)) = swap ? b : a;
+            *reinterpret_cast<uint4*>(chunk + (swap ? oa : ob)) = swap ? a : b;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kRounds; ++r) {
+            uint32_t o[8];
+            dequant_fp4_16(buf[qq].data[r].x, buf[qq].data[r].y, buf[qq].scale[r], o);
+            const uint32_t row = row0 + r * 4;
+            const uint32_t oa = swz<128>(row * 128 + u0 * 16);
+            const uint32_t ob = swz<128>(row * 128 + (u0 + 1) * 16);
+            const uint4 a = make_uint4(o[0], o[1], o[2], o[3]);
+            const uint4 b = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(chunk + (swap ? ob : oa)) = swap ? b : a;
+            *reinterpret_cast<uint4*>(chunk + (swap ? oa : ob)) = swap ? a : b;
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kQFull]);
+        if (lane == 0) mbar_arrive(&bars[kQuarterFull + qq]);
+        // The registers of this quarter now take the next tile's bytes.
+        if (g + 1 < span.g_end) load_quarter(p, nxt, qq, s8, buf[qq]);
+      }
+      cur = nxt;
+      nxt = nxt2;
+    }
+  } else {
+    // ------------------------------------------------------------------
+    // Softmax (+ tensor-core issue by thread 0) and epilogue.
+    // ------------------------------------------------------------------
+    const int i = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // TMEM columns: S^T [0, NH), O^T quarters [NH, 5 NH), row sums [5 NH, 6 NH).
+    const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + NH, tL = tmem + lane_base + 5 * NH;
+    constexpr int V = NH >= 32 ? NH / 32 : 1;  // values a lane keeps after a reduce-scatter
+    constexpr uint32_t idesc_qk = make_idesc_bf16(128, NH, false, false);
+    constexpr uint32_t idesc_pv = make_idesc_bf16(128, NH, true, true);
+    constexpr uint32_t p_sbo = 8 * 2 * NH;        // 8 rows of P^T
+    constexpr uint32_t p_swz = NH == 64 ? kSwizzle128 : (NH == 32 ? kSwizzle64 : kSwizzle32);
+    const uint32_t kv_base = smem_u32(sKV), q_base = smem_u32(sQ), p_base = smem_u32(sP);
+    uint32_t n_tile = 0, n_seg = 0;
+    bool issued = false;
+    for (int64_t g = span.g_begin; g < span.g_end;) {
+      const int qidx = static_cast<int>(g / p.T);
+      const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
+      const int64_t seg_begin = g;
+      {
+        uint32_t z[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) z[k] = 0u;
+#pragma unroll
+        for (int c = 0; c < NH / 16; ++c) tmem_st16(tL + c * 16, z);
+        tmem_wait_st();
       }
       for (; g < seg_end; ++g, ++n_tile) {
+        const bool first = g == seg_begin;
         const int t = static_cast<int>(g - static_cast<int64_t>(qidx) * p.T);
         const TileInfo ti = tile_info(p, qidx, t);
-        const uint8_t* rec[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int slot = ti.slot0 + pw * 32 + r * 4 + j4;
-          const int32_t id = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
-          const bool valid = id >= 0 && static_cast<int64_t>(id) < ti.pool;
-          if (!valid && id != -1 && hg == 0 && s8 == 0 && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_INDEX);
-          rec[r] = !valid ? nullptr
-                          : (ti.extra ? p.xkv + static_cast<int64_t>(id) * kRecFp4
-                                      : p.kv + static_cast<int64_t>(id) * kRecFp8);
-        }
-#pragma unroll 1
-        for (int qq = 0; qq < 4; ++qq) {
-          if (n_tile > 0) mbar_wait(&bars[kQuarterFree + qq], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitLimitNs);
-          // Store target: chunk 2qq + s8/4, row = token, 16-byte units
-          // 2(s8&3) and 2(s8&3)+1; lanes 4-7 of each quarter-warp store the
-          // odd unit first so that the 8 lanes of a phase hit 8 bank groups.
-          uint8_t* chunk = sKV + (2 * qq + (s8 >> 2)) * 16384;
-          const uint32_t u0 = 2 * (s8 & 3);
-          const bool swap = (s8 & 4) != 0;
-          auto store = [&](int r, const uint32_t (&o)[8]) {
-            const uint32_t row = pw * 32 + r * 4 + j4;
-            const uint4 a = make_uint4(o[0], o[1], o[2], o[3]);
-            const uint4 b = make_uint4(o[4], o[5], o[6], o[7]);
-            const uint32_t oa = swz<128>(row * 128 + u0 * 16);
-            const uint32_t ob = swz<128>(row * 128 + (u0 + 1) * 16);
-            *reinterpret_cast<uint4*>(chunk + (swap ? ob : oa)) = swap ? b : a;
-            *reinterpret_cast<uint4*>(chunk + (swap ? oa : ob)) = swap ? a : b;
-          };
-          if (!ti.extra) {
-            uint4 data[8];
-            uint32_t sw[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              if (rec[r]) {
-                data[r] = __ldg(reinterpret_cast<const uint4*>(rec[r] + qq * 128 + s8 * 16));
-                sw[r] = __ldg(reinterpret_cast<const uint32_t*>(rec[r] + 512 + qq * 4));
-              } else {
-                data[r] = make_uint4(0, 0, 0, 0);
-                sw[r] = 127u * 0x01010101u;
-              }
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              uint32_t o[8];
-              dequant_fp8_16(data[r], (sw[r] >> (8 * (s8 >> 1))) & 0xFFu, o);
-              store(r, o);
-            }
-          } else {
-            uint2 data[8];
-            uint32_t sb[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              if (rec[r]) {
-                data[r] = __ldg(reinterpret_cast<const uint2*>(rec[r] + qq * 64 + s8 * 8));
-                sb[r] = __ldg(rec[r] + 256 + qq * 8 + s8);
-              } else {
-                data[r] = make_uint2(0, 0);
-                sb[r] = 0x38u;  // 1.0
-              }
-            }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-              uint32_t o[8];
-              dequant_fp4_16(data[r].x, data[r].y, sb[r], o);
-              store(r, o);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kQuarterFull + qq]);
-        }
-      }
-      ++n_seg;
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------
-    // Tensor-core issuer (one thread).
-    // ------------------------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(128, NH, false, false);
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, NH, true, true);
-      constexpr uint32_t p_row = 2 * NH;            // bytes per P^T row
-      constexpr uint32_t p_sbo = 8 * p_row;         // 8-row group
-      constexpr uint32_t p_swz = NH == 64 ? kSwizzle128 : (NH == 32 ? kSwizzle64 : kSwizzle32);
-      const uint32_t kv_base = smem_u32(sKV), q_base = smem_u32(sQ), p_base = smem_u32(sP);
-      const uint32_t tS = tmem, tO = tmem + NH;
-      uint32_t n_tile = 0, n_seg = 0;
-      bool issued = false;
-      for (int64_t g = span.g_begin; g < span.g_end;) {
-        const int qidx = static_cast<int>(g / p.T);
-        const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-        mbar_wait(&bars[kQFull], n_seg & 1, abort_flag, p.d_error, kWaitLimitNs);
-        bool first = true;
-        for (; g < seg_end; ++g, ++n_tile) {
+        const int slot = ti.slot0 + i;
+        const int32_t id = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
+        const bool valid = id >= 0 && static_cast<int64_t>(id) < ti.pool;
+
+        if (tid == 0) {
           // S^T = K Q^T over the 8 dim chunks, as quarters arrive.
+          if (first) mbar_wait(&bars[kQFull], n_seg & 1, abort_flag, p.d_error, kWaitLimitNs);
 #pragma unroll 1
           for (int qq = 0; qq < 4; ++qq) {
             mbar_wait(&bars[kQuarterFull + qq], n_tile & 1, abort_flag, p.d_error, kWaitLimitNs);
@@ -345,15 +450,146 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
               for (int k = 0; k < 4; ++k) {
                 const uint64_t a = make_smem_desc(kv_base + c * 16384 + k * 32, 16, 1024, kSwizzle128);
                 const uint64_t b = make_smem_desc(q_base + c * (NH * 128) + k * 32, 16, 1024, kSwizzle128);
-                mma_bf16_ss(tS, a, b, idesc_qk, (c | k) != 0);
+                mma_bf16_ss(tmem, a, b, idesc_qk, (c | k) != 0);
               }
             }
           }
           issued = true;
           mma_commit(&bars[kSFull]);
           if (g + 1 == seg_end) mma_commit(&bars[kQFree]);
-          // O^T += V^T P^T once the softmax has written P^T.
-          mbar_wait(&bars[kPFull], n_tile & 1, abort_flag, p.d_error, kWaitLimitNs);
+        }
+        mbar_wait(&bars[kSFull], n_tile & 1, abort_flag, p.d_error, kWaitLimitNs);
+        __syncwarp();
+        tc_fence_after();
+
+        // Pass 1: largest excess of a score over its head's running max.
+        float excess = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < NH / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tS + c * 16, r);
+          const float4* m4 = reinterpret_cast<const float4*>(sm_m + c * 16);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 m = m4[k4];
+            excess = fmaxf(excess, __uint_as_float(r[4 * k4 + 0]) * p.scale_log2 - m.x);
+            excess = fmaxf(excess, __uint_as_float(r[4 * k4 + 1]) * p.scale_log2 - m.y);
+            excess = fmaxf(excess, __uint_as_float(r[4 * k4 + 2]) * p.scale_log2 - m.z);
+            excess = fmaxf(excess, __uint_as_float(r[4 * k4 + 3]) * p.scale_log2 - m.w);
+          }
+        }
+        int move_max;
+        {
+          const int mine = valid && excess > kLazyRescale;
+          asm volatile(
+              "{\n\t.reg .pred pi, po;\n\t"
+              "setp.ne.s32 pi, %1, 0;\n\t"
+              "bar.red.or.pred po, 2, %2, pi;\n\t"
+              "selp.s32 %0, 1, 0, po;\n\t}"
+              : "=r"(move_max)
+              : "r"(mine), "r"(kSoftmaxThreads)
+              : "memory");
+        }
+        if (move_max) {
+          // Exact column maxima of this tile, 16 heads at a time.
+#pragma unroll
+          for (int c = 0; c < NH / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(tS + c * 16, r);
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = valid ? __uint_as_float(r[k]) * p.scale_log2 : -INFINITY;
+            ReduceScatter<16, 16>::run(v, lane, MaxOp());
+            if ((lane & 1) == 0) red[warp * NH + c * 16 + (lane >> 1)] = v[0];
+          }
+          named_bar_sync(1, kSoftmaxThreads);
+          int any_rescale = 0;
+          if (i < NH) {
+            const float mt = fmaxf(fmaxf(red[i], red[NH + i]), fmaxf(red[2 * NH + i], red[3 * NH + i]));
+            const float m_old = sm_m[i];
+            float alpha = 1.f;
+            if (mt > m_old + kLazyRescale || (m_old == -INFINITY && mt > -INFINITY)) {
+              alpha = m_old == -INFINITY ? 0.f : ex2_approx(m_old - mt);
+              any_rescale = m_old != -INFINITY;
+              sm_m[i] = mt;
+            }
+            sm_alpha[i] = alpha;
+          }
+          asm volatile(
+              "{\n\t.reg .pred pi, po;\n\t"
+              "setp.ne.s32 pi, %1, 0;\n\t"
+              "bar.red.or.pred po, 2, %2, pi;\n\t"
+              "selp.s32 %0, 1, 0, po;\n\t}"
+              : "=r"(any_rescale)
+              : "r"(any_rescale), "r"(kSoftmaxThreads)
+              : "memory");
+          if (any_rescale) {
+#pragma unroll 1
+            for (int c = 0; c < NH / 16; ++c) {
+              uint32_t o[16];
+              tmem_ld16(tL + c * 16, o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * sm_alpha[c * 16 + k]);
+              tmem_st16(tL + c * 16, o);
+            }
+            tmem_wait_st();
+            if (!first) {
+              // O^T[d, h] *= alpha[h]; the products so far are complete (the
+              // tensor core finished them before this tile's S^T).
+#pragma unroll 1
+              for (int r = 0; r < 4; ++r) {
+#pragma unroll
+                for (int c = 0; c < NH / 16; ++c) {
+                  uint32_t o[16];
+                  tmem_ld16(tO + r * NH + c * 16, o);
+#pragma unroll
+                  for (int k = 0; k < 16; ++k)
+                    o[k] = __float_as_uint(__uint_as_float(o[k]) * sm_alpha[c * 16 + k]);
+                  tmem_st16(tO + r * NH + c * 16, o);
+                }
+              }
+              tmem_wait_st();
+            }
+          }
+        }
+        // Pass 2: P = 2^(x - m), row i of P^T (MN-major, swizzled), row sums.
+#pragma unroll 1
+        for (int c = 0; c < NH / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(tS + c * 16, r);
+          uint32_t l[16];
+          tmem_ld16(tL + c * 16, l);
+          float pv[16];
+          const float4* m4 = reinterpret_cast<const float4*>(sm_m + c * 16);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 m = m4[k4];
+            const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int k = 4 * k4 + j;
+              const float xv = __uint_as_float(r[k]) * p.scale_log2 - mm[j];
+              pv[k] = (valid && mm[j] != -INFINITY) ? ex2_approx(xv) : 0.f;
+              l[k] = __float_as_uint(__uint_as_float(l[k]) + pv[k]);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(pv[8 * u + 0], pv[8 * u + 1]);
+            w.y = pack_bf16x2(pv[8 * u + 2], pv[8 * u + 3]);
+            w.z = pack_bf16x2(pv[8 * u + 4], pv[8 * u + 5]);
+            w.w = pack_bf16x2(pv[8 * u + 6], pv[8 * u + 7]);
+            *reinterpret_cast<uint4*>(sP + swz<2 * NH>(i * (2 * NH) + (2 * c + u) * 16)) = w;
+          }
+          tmem_st16(tL + c * 16, l);
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(1, kSoftmaxThreads);
+        if (tid == 0) {
+          // O^T += V^T P^T.
           tc_fence_after();
 #pragma unroll 1
           for (int r = 0; r < 4; ++r) {
@@ -361,139 +597,34 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
             for (int ks = 0; ks < 8; ++ks) {
               const uint64_t a = make_smem_desc(kv_base + 2 * r * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
               const uint64_t b = make_smem_desc(p_base + ks * 2 * p_sbo, 16 * p_sbo, p_sbo, p_swz);
-              mma_bf16_ss(tO + r * NH, a, b, idesc_pv, !(first && ks == 0));
+              mma_bf16_ss(tmem + NH + r * NH, a, b, idesc_pv, !(first && ks == 0));
             }
             mma_commit(&bars[kQuarterFree + r]);
           }
           if (g + 1 == seg_end) mma_commit(&bars[kOReady]);
-          first = false;
         }
-        ++n_seg;
       }
-      if (issued) {
-        // Normal runs have completed every product already (the softmax
-        // waited for it); after a timeout this keeps TMEM alive until the
-        // tensor core is done with it.
-        mma_commit(&bars[kDrain]);
-        mbar_wait(&bars[kDrain], 0, abort_flag, p.d_error, kWaitLimitNs);
-      }
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------------
-    // Softmax and epilogue: thread i <-> TMEM lane i.
-    // ------------------------------------------------------------------
-    const int i = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + NH;
-    constexpr int V = NH >= 32 ? NH / 32 : 1;  // values a lane keeps after a reduce-scatter
-    uint32_t n_tile = 0, n_seg = 0;
-    if (i < NH) sm_m[i] = -INFINITY;
-    for (int64_t g = span.g_begin; g < span.g_end;) {
-      const int qidx = static_cast<int>(g / p.T);
-      const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-      const int64_t seg_begin = g;
-      float lw[V];
-#pragma unroll
-      for (int k = 0; k < V; ++k) lw[k] = 0.f;
-      for (; g < seg_end; ++g, ++n_tile) {
-        const int t = static_cast<int>(g - static_cast<int64_t>(qidx) * p.T);
-        const TileInfo ti = tile_info(p, qidx, t);
-        const int slot = ti.slot0 + i;
-        const int32_t id = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
-        const bool valid = id >= 0 && static_cast<int64_t>(id) < ti.pool;
 
-        mbar_wait(&bars[kSFull], n_tile & 1, abort_flag, p.d_error, kWaitLimitNs);
-        tc_fence_after();
-        // Column max over the 128 tokens of the tile (reduce-scatter in place).
-        {
-          float v[NH];
-#pragma unroll
-          for (int c = 0; c < NH / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(tS + c * 16, r);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[c * 16 + k] = valid ? __uint_as_float(r[k]) * p.scale_log2 : -INFINITY;
-          }
-          ReduceScatter<NH, 16>::run(v, lane, MaxOp());
-#pragma unroll
-          for (int k = 0; k < V; ++k) red[warp * NH + rs_head<NH>(lane, k)] = v[k];
-        }
-        named_bar_sync(1, kSoftmaxThreads);
-        int need = 0;
-        if (i < NH) {
-          const float mt = fmaxf(fmaxf(red[i], red[NH + i]), fmaxf(red[2 * NH + i], red[3 * NH + i]));
-          const float m_old = sm_m[i];
-          float alpha = 1.f;
-          if (mt > m_old + kLazyRescale || (m_old == -INFINITY && mt > -INFINITY)) {
-            alpha = m_old == -INFINITY ? 0.f : ex2_approx(m_old - mt);
-            need = m_old != -INFINITY;
-            sm_m[i] = mt;
-          }
-          sm_alpha[i] = alpha;
-        }
-        int any_rescale;
-        asm volatile(
-            "{\n\t.reg .pred pi, po;\n\t"
-            "setp.ne.s32 pi, %1, 0;\n\t"
-            "bar.red.or.pred po, 2, %2, pi;\n\t"
-            "selp.s32 %0, 1, 0, po;\n\t}"
-            : "=r"(any_rescale)
-            : "r"(need), "r"(kSoftmaxThreads)
-            : "memory");
-        // P = 2^(x - m) (S re-read from TMEM), stored as row i of P^T
-        // (MN-major, swizzled), then its column sums.
-        {
-          float v[NH];
-#pragma unroll
-          for (int c = 0; c < NH / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(tS + c * 16, r);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float m = sm_m[c * 16 + k];
-              const float xv = __uint_as_float(r[k]) * p.scale_log2;
-              v[c * 16 + k] = (!valid || m == -INFINITY) ? 0.f : ex2_approx(xv - m);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < NH / 8; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(v[8 * u + 0], v[8 * u + 1]);
-            w.y = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
-            w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
-            w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
-            *reinterpret_cast<uint4*>(sP + swz<2 * NH>(i * (2 * NH) + u * 16)) = w;
-          }
-          ReduceScatter<NH, 16>::run(v, lane, AddOp());
-#pragma unroll
-          for (int k = 0; k < V; ++k) lw[k] = lw[k] * sm_alpha[rs_head<NH>(lane, k)] + v[k];
-        }
-        if (any_rescale) {
-          // O^T[d, h] *= alpha[h]; the previous products are complete
-          // (the tensor core finished them before this tile's S^T).
-#pragma unroll 1
-          for (int r = 0; r < 4; ++r) {
-#pragma unroll
-            for (int c = 0; c < NH / 16; ++c) {
-              uint32_t o[16];
-              tmem_ld16(tO + r * NH + c * 16, o);
-              #pragma unroll
-              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * sm_alpha[c * 16 + k]);
-              tmem_st16(tO + r * NH + c * 16, o);
-            }
-          }
-          tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bars[kPFull]);
-      }
       // Epilogue of this query token (or of this split of it).
-      mbar_wait(&bars[kOReady], n_seg & 1, abort_flag, p.d_error, kWaitLimitNs);
-      tc_fence_after();
+      // Column sums of the per-thread row sums.
+      {
+        float lw[NH];
 #pragma unroll
-      for (int k = 0; k < V; ++k) red[warp * NH + rs_head<NH>(lane, k)] = lw[k];
+        for (int c = 0; c < NH / 16; ++c) {
+          uint32_t l[16];
+          tmem_ld16(tL + c * 16, l);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) lw[c * 16 + k] = __uint_as_float(l[k]);
+        }
+        ReduceScatter<NH, 16>::run(lw, lane, AddOp());
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+          if (NH >= 32 || (lane & 1) == 0) red[warp * NH + rs_head<NH>(lane, k)] = lw[k];
+        }
+      }
+      mbar_wait(&bars[kOReady], n_seg & 1, abort_flag, p.d_error, kWaitLimitNs);
+      __syncwarp();
+      tc_fence_after();
       named_bar_sync(1, kSoftmaxThreads);
       const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
       const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
@@ -521,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
         for (int c = 0; c < NH / 16; ++c) {
           uint32_t o[16];
           tmem_ld16(tO + r * NH + c * 16, o);
-          #pragma unroll
+#pragma unroll
           for (int k = 0; k < 16; ++k) {
             const int h = c * 16 + k;
             const float v = __uint_as_float(o[k]) * sm_linv[h];
@@ -535,16 +666,43 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(const Decode
         }
       }
       tc_fence_before();
+      named_bar_sync(1, kSoftmaxThreads);  // O and sm_m reads done before the next token's tiles
       ++n_seg;
+    }
+    if (tid == 0 && issued) {
+      // Normal runs have completed every product already (the epilogue
+      // waited for it); after a timeout this keeps TMEM alive until the
+      // tensor core is done with it.
+      mma_commit(&bars[kDrain]);
+      mbar_wait(&bars[kDrain], 0, abort_flag, p.d_error, kWaitLimitNs);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    tried = true;
+  }
+  return fn;
 }
 
 }  // namespace
@@ -558,7 +716,19 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  sparse_decode_kernel<NH><<<grid, kThreads, smem, stream>>>(p);
+  // Q viewed as [nq * h_q rows][512 bf16]; a box is NH rows x 64 dims, 128-byte swizzled.
+  EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap q_map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.nq) * p.h_q};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(NH)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  sparse_decode_kernel<NH><<<grid, kThreads, smem, stream>>>(p, q_map);
   return cudaGetLastError();
 }
 
