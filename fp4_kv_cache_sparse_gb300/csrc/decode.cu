@@ -209,14 +209,16 @@ __device__ __forceinline__ TileInfo tile_info(const DecodeParams& p, int qidx, i
   return ti;
 }
 
-// One producer lane's view of a tile: its 4 token slots (one per load
-// round), each -1 when there is nothing to load.
+// One producer lane's view of a tile: the raw index of its token in each
+// load round (-1 past the end of the row), fetched two tiles ahead and only
+// checked against the pool when its bytes are requested, one tile later, so
+// that the index loads' latency stays hidden.
 struct LaneTile {
   int32_t id[kRounds];
   bool extra;
 };
 
-__device__ __forceinline__ LaneTile lane_tile(const DecodeParams& p, int64_t g, int row0, bool flag_bad) {
+__device__ __forceinline__ LaneTile lane_tile(const DecodeParams& p, int64_t g, int row0) {
   LaneTile lt;
   const int qidx = static_cast<int>(g / p.T);
   const TileInfo ti = tile_info(p, qidx, static_cast<int>(g - static_cast<int64_t>(qidx) * p.T));
@@ -224,12 +226,21 @@ __device__ __forceinline__ LaneTile lane_tile(const DecodeParams& p, int64_t g, 
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
     const int slot = ti.slot0 + row0 + r * 4;
-    const int32_t id = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
-    const bool valid = id >= 0 && static_cast<int64_t>(id) < ti.pool;
+    lt.id[r] = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
+  }
+  return lt;
+}
+
+// Entries outside [0, pool) become -1 (skipped); all but -1 are flagged.
+__device__ __forceinline__ void validate(const DecodeParams& p, LaneTile& lt, bool flag_bad) {
+  const int64_t pool = lt.extra ? p.xpool_tokens : p.pool_tokens;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int32_t id = lt.id[r];
+    const bool valid = id >= 0 && static_cast<int64_t>(id) < pool;
     if (!valid && id != -1 && flag_bad && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_INDEX);
     lt.id[r] = valid ? id : -1;
   }
-  return lt;
 }
 
 // Register-resident bytes of one quarter (128 dims) of the lane's 4 tokens.
@@ -238,7 +249,9 @@ struct QuarterRegs {
   uint32_t scale[kRounds];
 };
 
-__device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTile& lt, int qq, int s8,
+// seg = 16-dim segment of the lane within the quarter (0..7): dims
+// 128 qq + 16 seg .. +15.
+__device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTile& lt, int qq, int seg,
                                              QuarterRegs& q) {
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
@@ -248,13 +261,13 @@ __device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTi
       q.scale[r] = lt.extra ? 0x38u : 127u * 0x01010101u;
     } else if (!lt.extra) {
       const uint8_t* rec = p.kv + static_cast<int64_t>(id) * kRecFp8;
-      q.data[r] = ldg_stream16(rec + qq * 128 + s8 * 16);
+      q.data[r] = ldg_stream16(rec + qq * 128 + seg * 16);
       q.scale[r] = ldg_u32(rec + 512 + qq * 4);
     } else {
       const uint8_t* rec = p.xkv + static_cast<int64_t>(id) * kRecFp4;
-      const uint2 d = ldg_stream8(rec + qq * 64 + s8 * 8);
+      const uint2 d = ldg_stream8(rec + qq * 64 + seg * 8);
       q.data[r] = make_uint4(d.x, d.y, 0, 0);
-      q.scale[r] = ldg_u8(rec + 256 + qq * 8 + s8);
+      q.scale[r] = ldg_u8(rec + 256 + qq * 8 + seg);
     }
   }
 }
@@ -311,25 +324,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Producers.
     // ------------------------------------------------------------------
     const int pw = warp - 4;
-    const int j4 = lane >> 3;  // token of the 4 one load instruction covers
-    const int s8 = lane & 7;   // 16-dim segment within a 128-dim quarter
-    const int row0 = pw * kRowsPerProducerWarp + j4;
-    const bool flag_bad = hg == 0 && s8 == 0;
-    // Store geometry: chunk 2qq + s8/4, 16-byte units 2(s8&3), +1; lanes
-    // 4-7 of a quarter-warp store the odd unit first so the 8 lanes of a
-    // store phase hit 8 different bank groups.
-    const uint32_t u0 = 2 * (s8 & 3);
-    const bool swap = (s8 & 4) != 0;
+    // Lane geometry: lane = c1 * 16 + t4 * 4 + s4.  A load instruction
+    // covers 4 tokens (t4) x 2 chunks of the quarter (c1) x 4 16-byte
+    // segments (s4); a store phase (8 consecutive lanes) covers two adjacent
+    // rows, whose different swizzle patterns put the 8 stores in 8 different
+    // bank groups.
+    const int s4 = lane & 3;
+    const int t4 = (lane >> 2) & 3;
+    const int c1 = lane >> 4;
+    const int seg = c1 * 4 + s4;        // 16-dim segment within the quarter
+    const int row0 = pw * kRowsPerProducerWarp + t4;
+    const bool flag_bad = hg == 0 && seg == 0;
+    // Byte offsets of the lane's two 16-byte units in its chunk for row
+    // row0 + 4 r: the row's low 3 bits are t4 + 4 (r & 1).
+    uint32_t off_even[2], off_odd[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint32_t row = row0 + 4 * rr;
+      off_even[rr] = swz<128>(row * 128 + (2 * s4) * 16);
+      off_odd[rr] = swz<128>(row * 128 + (2 * s4 + 1) * 16);
+    }
+    const int sshift = 8 * (2 * c1 + (s4 >> 1));  // scale byte within the quarter's scale word
 
     uint32_t n_tile = 0, n_seg = 0;
     int64_t g = span.g_begin;
     LaneTile cur{}, nxt{};
     QuarterRegs buf[4];
     if (g < span.g_end) {
-      cur = lane_tile(p, g, row0, flag_bad);
-      if (g + 1 < span.g_end) nxt = lane_tile(p, g + 1, row0, flag_bad);
+      cur = lane_tile(p, g, row0);
+      validate(p, cur, flag_bad);
+      if (g + 1 < span.g_end) nxt = lane_tile(p, g + 1, row0);
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) load_quarter(p, cur, qq, s8, buf[qq]);
+      for (int qq = 0; qq < 4; ++qq) load_quarter(p, cur, qq, seg, buf[qq]);
     }
     int64_t seg_end = g;  // forces a segment start on the first tile
     for (; g < span.g_end; ++g, ++n_tile) {
@@ -349,19 +375,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool extra = cur.extra;
       LaneTile nxt2{};
-      if (g + 2 < span.g_end) nxt2 = lane_tile(p, g + 2, row0, flag_bad);
+      if (g + 2 < span.g_end) nxt2 = lane_tile(p, g + 2, row0);
+      if (g + 1 < span.g_end) validate(p, nxt, flag_bad);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         if (n_tile > 0) mbar_wait(&bars[kQuarterFree + qq], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitLimitNs);
-        uint8_t* chunk = sKV + (2 * qq + (s8 >> 2)) * 16384;
+        uint8_t* chunk = sKV + (2 * qq + c1) * 16384;
         if (!extra) {
           uint32_t sb[kRounds];
+          bool big = false;
 #pragma unroll
-          for (int r = 0; r < kRounds; ++r) sb[r] = (buf[qq].scale[r] >> (8 * (s8 >> 1))) & 0xFFu;
-          bool any_big = false;
-#pragma unroll
-          for (int r = 0; r < kRounds; ++r) any_big |= sb[r] > 142u;
-          any_big = __any_sync(0xFFFFFFFFu, any_big);
+          for (int r = 0; r < kRounds; ++r) {
+            sb[r] = (buf[qq].scale[r] >> sshift) & 0xFFu;
+            big |= sb[r] > 142u;
+          }
+          const bool any_big = __any_sync(0xFFFFFFFFu, big);
 #pragma unroll
           for (int r = 0; r < kRounds; ++r) {
             uint32_t o[8];
@@ -369,33 +397,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               dequant_fp8_16_small_scale(buf[qq].data[r], sb[r], o);
             else
               dequant_fp8_16(buf[qq].data[r], sb[r], o);
-            const uint32_t row = row0 + r * 4;
-            const uint32_t oa = swz<128>(row * 128 + u0 * 16);
-            const uint32_t ob = swz<128>(row * 128 + (u0 + 1) * 16);
-            const uint4 a = make_uint4(o[0], o[1], o[2], o[3]);
-            const uint4 b = make_uint4(o[4], o[5], o[6], o[7]);
-            *reinterpret_cast<uint4*>(chunk + (swap ? ob : oa)) = swap ? b : a;
-            *reinterpret_cast<uint4*>(chunk + (swap ? oa : ob)) = swap ? a : b;
+            const uint32_t radd = (r >> 1) * 1024;  // rows r and r + 2 differ by 8 rows
+            *reinterpret_cast<uint4*>(chunk + off_even[r & 1] + radd) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(chunk + off_odd[r & 1] + radd) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         } else {
 #pragma unroll
           for (int r = 0; r < kRounds; ++r) {
             uint32_t o[8];
             dequant_fp4_16(buf[qq].data[r].x, buf[qq].data[r].y, buf[qq].scale[r], o);
-            const uint32_t row = row0 + r * 4;
-            const uint32_t oa = swz<128>(row * 128 + u0 * 16);
-            const uint32_t ob = swz<128>(row * 128 + (u0 + 1) * 16);
-            const uint4 a = make_uint4(o[0], o[1], o[2], o[3]);
-            const uint4 b = make_uint4(o[4], o[5], o[6], o[7]);
-            *reinterpret_cast<uint4*>(chunk + (swap ? ob : oa)) = swap ? b : a;
-            *reinterpret_cast<uint4*>(chunk + (swap ? oa : ob)) = swap ? a : b;
+            const uint32_t radd = (r >> 1) * 1024;
+            *reinterpret_cast<uint4*>(chunk + off_even[r & 1] + radd) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(chunk + off_odd[r & 1] + radd) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kQuarterFull + qq]);
         // The registers of this quarter now take the next tile's bytes.
-        if (g + 1 < span.g_end) load_quarter(p, nxt, qq, s8, buf[qq]);
+        if (g + 1 < span.g_end) load_quarter(p, nxt, qq, seg, buf[qq]);
       }
       cur = nxt;
       nxt = nxt2;
