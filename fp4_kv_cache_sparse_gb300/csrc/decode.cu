@@ -11,8 +11,7 @@
 // contiguous run of (query token, 128-slot tile) work items:
 //   warps 4-11  producers.  Each warp owns 16 token rows of a tile.  Record
 //               bytes are loaded with 16-byte read-only loads one whole tile
-//               ahead (registers, issued as one batch after the last quarter
-//               of a tile is published), indices two tiles ahead; a quarter (128
+//               ahead (registers), indices two tiles ahead; a quarter (128
 //               dims) is dequantized exactly to bf16 in registers and stored
 //               into shared memory in the 128-byte-swizzled canonical layout
 //               as soon as the tensor core has released that quarter.
@@ -375,6 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++n_seg;
       }
       const bool extra = cur.extra;
+      LaneTile nxt2{};
+      if (g + 2 < span.g_end) nxt2 = lane_tile(p, g + 2, row0);
+      if (g + 1 < span.g_end) validate(p, nxt, flag_bad);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         if (n_tile > 0) mbar_wait(&bars[kQuarterFree + qq], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitLimitNs);
@@ -409,23 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(chunk + off_odd[r & 1] + radd) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
-        // Publishing the quarter (proxy fence + release arrive) waits for
-        // every memory access this thread has in flight, so no global load
-        // is issued between the first and the last publication of a tile.
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kQuarterFull + qq]);
+        // The registers of this quarter now take the next tile's bytes.
+        if (g + 1 < span.g_end) load_quarter(p, nxt, qq, seg, buf[qq]);
       }
-      // All four quarters of the next tile, and the indices of the one
-      // after, in one batch: they arrive while the tensor core finishes this
-      // tile and before the next tile's first quarter slot is released.
-      LaneTile nxt2{};
-      if (g + 1 < span.g_end) {
-        validate(p, nxt, flag_bad);
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) load_quarter(p, nxt, qq, seg, buf[qq]);
-      }
-      if (g + 2 < span.g_end) nxt2 = lane_tile(p, g + 2, row0);
       cur = nxt;
       nxt = nxt2;
     }
