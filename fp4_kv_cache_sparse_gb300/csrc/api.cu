@@ -189,10 +189,16 @@ mla_status_t mla_sparse_decode(const mla_problem_t* problem, const void* q, cons
 
   const int grid = pl.num_parts * pl.n_hg;
   cudaError_t e;
-  switch (pl.nh) {
-    case 64: e = launch_decode<64>(p, grid, s); break;
-    case 32: e = launch_decode<32>(p, grid, s); break;
-    default: e = launch_decode<16>(p, grid, s); break;
+  if (problem->h_q == 128 && problem->extra_topk == 0) {
+    // All 128 heads on the MMA's M dimension, the latent dims split over a
+    // 2-CTA cluster (same part count and SM budget as two 64-head groups).
+    e = launch_decode_pair(p, pl.num_parts, s);
+  } else {
+    switch (pl.nh) {
+      case 64: e = launch_decode<64>(p, grid, s); break;
+      case 32: e = launch_decode<32>(p, grid, s); break;
+      default: e = launch_decode<16>(p, grid, s); break;
+    }
   }
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   if (pl.num_parts > 1) {

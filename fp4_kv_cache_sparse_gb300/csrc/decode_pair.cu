@@ -1,0 +1,706 @@
+// decode_pair.cu -- token-sparse MLA decode for 128 query heads on a cluster of
+// two CTAs that split the 512 latent dims (sm_103a: tcgen05 + TMEM + TMA +
+// distributed shared memory).
+//
+// What it computes is the same as decode.cu ("flops/flashmla-decode-fp8-fp4-kv",
+// "Arithmetic intensity" and "Workarounds"; "deepseek-ai/FlashMLA", "How to use
+// it"), for an FP8 main cache without an extra cache.  The layout differs:
+// heads are the MMA's M dimension (all 128 of them), so both products run on
+// the tensor core at full rate -- S = Q K^T with N = 128 tokens and
+// O = P V with N = 128 dims per instruction -- instead of the 64-head,
+// tokens-on-M form whose small N leaves the tensor core waiting on shared
+// memory.  O for 128 heads x 512 dims would fill all of TMEM, so CTA c of the
+// pair owns dims [256c, 256c + 256): its half of every record, of Q, of the
+// bf16 tile and of O.  Each CTA's S is a partial sum over its half; the halves
+// are exchanged through distributed shared memory:
+//   - S: CTA c owns the softmax of heads [64c, 64c + 64); the two warps whose
+//     TMEM lanes hold the other 64 heads ship those rows of the partial S to
+//     the peer ("shippers"), the owners add the peer's rows to their own.
+//   - P: owners write their rows of P (bf16) into both CTAs' P operand, plus
+//     the rescale factor alpha of each of their heads; shippers apply the
+//     peer's alpha to their O rows.
+//   - 1/l at the end of a query token goes the same way.
+// Records reach shared memory by TMA row gathers (tile::gather4, 4 tokens per
+// instruction, 64 bytes of one record's dim chunk per row) into a 3-slot
+// staging ring, so the dequantizing warps never have global loads in flight
+// when they publish a chunk.
+//
+// Warps: 0-3 softmax (thread i <-> head i <-> TMEM lane i), 4-11 dequant,
+// 12 loader (indices, validity mask, all TMA), 13 tensor-core issuer.
+#include <cstdint>
+#include <cuda.h>
+
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kPThreads = 448;
+constexpr int kHeads = 128;
+constexpr int kHalf = 256;
+constexpr int kStgSlots = 3;
+constexpr int kProdWarps = 8;
+constexpr int kLoaderWarp = 12;
+constexpr int kIssueWarp = 13;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLazy = 8.0f;
+
+struct PairSmem {
+  static constexpr int kQ = 0;                   // 4 chunks x [128 heads x 128 B], SW128
+  static constexpr int kKV = kQ + 65536;         // 4 chunks x [128 tokens x 128 B], SW128
+  static constexpr int kP = kKV + 65536;         // 2 chunks x [128 heads x 128 B] (64 tokens each)
+  static constexpr int kX = kP + 32768;          // [64 heads][128 tokens] fp32 from the peer
+  static constexpr int kStg = kX + 32768;        // 3 slots x [128 tokens x 64 B] raw e4m3
+  static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [32 groups x 128 B]: 4 tokens x 16 B scales
+  static constexpr int kBar = kScl + 2 * 4096;   // 40 mbarriers
+  static constexpr int kMask = kBar + 40 * 8;    // [2][4] u32 validity bits
+  static constexpr int kAlpha = kMask + 32;      // [64] f32, from the peer
+  static constexpr int kStats = kAlpha + 256;    // [2][64] f32 (1/l), from the peer
+  static constexpr int kScalar = kStats + 512;   // tmem slot, abort flag
+  static constexpr int kEnd = kScalar + 64;
+  static constexpr int kAlloc = kEnd + 1024;
+};
+
+enum PairBar {
+  bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
+  bKvFull = 14, bKvFree = 18, bQFull = 20, bQFree = 21, bSFull = 22, bXFull = 23, bXFree = 24,
+  bPIn = 25, bPFull = 26, bPvLocal = 27, bPvPeer = 28, bOReady = 29, bStatsIn = 30, bDrain = 32
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t peer_of(uint32_t local, uint32_t peer) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(peer));
+  return r;
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// Wait on a barrier that the peer CTA arrives on (cluster-scope acquire).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  int32_t* d_error) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63) == 63) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        if (d_error) atomicOr(d_error, MLA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// Four rows (tokens) of a 2-D byte tensor, x bytes in, into consecutive rows of dst.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%"
+      "29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct PSpan {
+  int64_t g_begin, g_end;
+  int first_local_split;
+  bool ok;
+};
+
+__device__ __forceinline__ PSpan pair_span(const DecodeParams& p, int part) {
+  PSpan s;
+  const int32_t* e = p.sched + static_cast<int64_t>(part) * MLA_SCHED_INTS;
+  s.g_begin = e[0];
+  s.g_end = e[1];
+  s.first_local_split = e[2];
+  const int64_t G = static_cast<int64_t>(p.nq) * p.T;
+  s.ok = s.g_begin >= 0 && s.g_begin <= s.g_end && s.g_end <= G && s.first_local_split >= 0;
+  if (!s.ok) s.g_begin = s.g_end = 0;
+  return s;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
+    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap q_map,
+                              const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap scl_map) {
+  using L = PairSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sKV = smem + L::kKV;
+  uint8_t* sP = smem + L::kP;
+  float* sX = reinterpret_cast<float*>(smem + L::kX);
+  uint8_t* sStg = smem + L::kStg;
+  uint8_t* sScl = smem + L::kScl;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + L::kMask);
+  float* sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
+  float* sStats = reinterpret_cast<float*>(smem + L::kStats);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kScalar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kScalar + 4);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t c = cluster_rank();
+  const uint32_t peer = c ^ 1u;
+  const int part = blockIdx.x >> 1;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStgSlots; ++i) {
+      mbar_init(&bars[bStgFull + i], 1);
+      mbar_init(&bars[bStgFree + i], kProdWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[bSclFull + i], 1);
+      mbar_init(&bars[bSclFree + i], kProdWarps);
+      mbar_init(&bars[bMaskFull + i], 1);
+      mbar_init(&bars[bMaskFree + i], 64);
+      mbar_init(&bars[bKvFree + i], 1);
+      mbar_init(&bars[bStatsIn + i], 64);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[bKvFull + i], kProdWarps);
+    mbar_init(&bars[bQFull], 1);
+    mbar_init(&bars[bQFree], 1);
+    mbar_init(&bars[bSFull], 1);
+    mbar_init(&bars[bXFull], 64);
+    mbar_init(&bars[bXFree], 64);
+    mbar_init(&bars[bPIn], 64);
+    mbar_init(&bars[bPFull], 128);
+    mbar_init(&bars[bPvLocal], 1);
+    mbar_init(&bars[bPvPeer], 1);
+    mbar_init(&bars[bOReady], 1);
+    mbar_init(&bars[bDrain], 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers exist before anyone arrives on them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const PSpan span = pair_span(p, part);
+  if (!span.ok && tid == 0 && c == 0 && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_METADATA);
+
+  if (warp == kLoaderWarp) {
+    // ------------------------------------------------------------------
+    // Loader: indices -> validity mask, TMA gathers of record halves, Q.
+    // Lane l covers tokens 4l .. 4l+3 of a tile.
+    // ------------------------------------------------------------------
+    uint32_t n_tile = 0, n_seg = 0, n_chunk = 0;
+    int64_t seg_end = span.g_begin;
+    auto raw_ids = [&](int64_t g, int32_t (&id)[4]) {
+      const int qidx = static_cast<int>(g / p.T);
+      const int t = static_cast<int>(g - static_cast<int64_t>(qidx) * p.T);
+      const int32_t* ids = p.idx + static_cast<int64_t>(qidx) * p.topk;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int slot = t * kTile + 4 * lane + j;
+        id[j] = slot < p.topk ? __ldg(ids + slot) : -1;
+      }
+    };
+    int32_t cur[4] = {-1, -1, -1, -1}, nxt[4] = {-1, -1, -1, -1};
+    if (span.g_begin < span.g_end) raw_ids(span.g_begin, cur);
+    if (span.g_begin + 1 < span.g_end) raw_ids(span.g_begin + 1, nxt);
+    for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
+      int32_t nxt2[4] = {-1, -1, -1, -1};
+      if (g + 2 < span.g_end) raw_ids(g + 2, nxt2);
+      if (g == seg_end) {
+        const int qidx = static_cast<int>(g / p.T);
+        seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
+        if (lane == 0) {
+          if (n_seg > 0) mbar_wait(&bars[bQFree], (n_seg - 1) & 1, abort_flag, p.d_error, kWaitNs);
+          mbar_expect_tx(&bars[bQFull], kHeads * kHalf * 2);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tma_load_2d(sQ + k * 16384, &q_map, static_cast<int>(c) * kHalf + k * 64, qidx * kHeads, &bars[bQFull]);
+        }
+        ++n_seg;
+      }
+      // Validity; rows for the gathers (-1 = out of the tensor: zero fill).
+      int32_t row[4];
+      uint32_t vbits[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int32_t id = cur[j];
+        const bool valid = id >= 0 && static_cast<int64_t>(id) < p.pool_tokens;
+        if (!valid && id != -1 && c == 0 && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_INDEX);
+        row[j] = valid ? id : -1;
+        vbits[j] = __ballot_sync(0xFFFFFFFFu, valid);
+      }
+      const uint32_t mp = n_tile & 1;
+      if (lane == 0) {
+        if (n_tile >= 2) mbar_wait(&bars[bMaskFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sMask[mp * 4 + j] = vbits[j];
+        mbar_arrive(&bars[bMaskFull + mp]);
+        if (n_tile >= 2) mbar_wait(&bars[bSclFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
+        mbar_expect_tx(&bars[bSclFull + mp], 32 * 64);
+      }
+      __syncwarp();
+      tma_gather4(sScl + mp * 4096 + lane * 128, &scl_map, 512, row[0], row[1], row[2], row[3],
+                  &bars[bSclFull + mp]);
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k, ++n_chunk) {
+        const uint32_t slot = n_chunk % kStgSlots, use = n_chunk / kStgSlots;
+        if (lane == 0) {
+          if (use > 0) mbar_wait(&bars[bStgFree + slot], (use - 1) & 1, abort_flag, p.d_error, kWaitNs);
+          mbar_expect_tx(&bars[bStgFull + slot], 32 * 256);
+        }
+        __syncwarp();
+        tma_gather4(sStg + slot * 8192 + lane * 256, &kv_map, static_cast<int>(c) * kHalf + k * 64, row[0], row[1],
+                    row[2], row[3], &bars[bStgFull + slot]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        cur[j] = nxt[j];
+        nxt[j] = nxt2[j];
+      }
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------------
+    // Dequantizers: staging (raw e4m3 + e8m0) -> bf16 tile chunk.
+    // Lane L (0..255) handles items L and L + 256 of a chunk; item i is
+    // token i >> 2, 16-dim segment i & 3.
+    // ------------------------------------------------------------------
+    const int L = tid - 128;
+    uint32_t n_tile = 0, n_chunk = 0;
+    for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
+      const uint32_t mp = n_tile & 1;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k, ++n_chunk) {
+        const uint32_t slot = n_chunk % kStgSlots, use = n_chunk / kStgSlots;
+        if (k == 0) mbar_wait(&bars[bSclFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+        mbar_wait(&bars[bStgFull + slot], use & 1, abort_flag, p.d_error, kWaitNs);
+        if ((k & 1) == 0 && n_tile > 0)
+          mbar_wait(&bars[bKvFree + (k >> 1)], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitNs);
+        const uint8_t* stg = sStg + slot * 8192;
+        const uint8_t* scl = sScl + mp * 4096;
+        uint8_t* chunk = sKV + k * 16384;
+        uint4 raw[2];
+        uint32_t sb[2];
+        bool big = false;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int item = L + 256 * r;
+          const int t = item >> 2, s = item & 3;
+          raw[r] = *reinterpret_cast<const uint4*>(stg + t * 64 + s * 16);
+          sb[r] = scl[(t >> 2) * 128 + (t & 3) * 16 + c * 8 + k * 2 + (s >> 1)];
+          big |= sb[r] > 142u;
+        }
+        const bool any_big = __any_sync(0xFFFFFFFFu, big);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int item = L + 256 * r;
+          const int t = item >> 2, s = item & 3;
+          uint32_t o[8];
+          if (!any_big)
+            dequant_fp8_16_small_scale(raw[r], sb[r], o);
+          else
+            dequant_fp8_16(raw[r], sb[r], o);
+          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (2 * s) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (2 * s + 1) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[bKvFull + k]);
+          mbar_arrive(&bars[bStgFree + slot]);
+          if (k == 3) mbar_arrive(&bars[bSclFree + mp]);
+        }
+      }
+    }
+  } else if (warp == kIssueWarp) {
+    // ------------------------------------------------------------------
+    // Tensor-core issue (one thread).
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
+      const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+      const uint32_t tS = tmem, tO = tmem + 128;
+      const uint32_t peer_pv = peer_of(smem_u32(&bars[bPvPeer]), peer);
+      uint32_t n_tile = 0, n_seg = 0;
+      bool issued = false;
+      for (int64_t g = span.g_begin; g < span.g_end;) {
+        const int qidx = static_cast<int>(g / p.T);
+        const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
+        mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
+        bool first = true;
+        for (; g < seg_end; ++g, ++n_tile) {
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            mbar_wait(&bars[bKvFull + k], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = make_smem_desc(q_base + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
+              const uint64_t b = make_smem_desc(kv_base + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
+              mma_bf16_ss(tS, a, b, idesc_qk, (k | kk) != 0);
+            }
+          }
+          issued = true;
+          mma_commit(&bars[bSFull]);
+          if (g + 1 == seg_end) mma_commit(&bars[bQFree]);
+          mbar_wait(&bars[bPFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          tc_fence_after();
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t a = make_smem_desc(p_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128);
+              const uint64_t b = make_smem_desc(kv_base + 2 * hh * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
+              mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(first && ks == 0));
+            }
+            mma_commit(&bars[bKvFree + hh]);
+          }
+          mma_commit(&bars[bPvLocal]);
+          if (g + 1 == seg_end) mma_commit(&bars[bOReady]);
+          // Tell the peer that this CTA's P operand is free again.
+          mbar_wait(&bars[bPvLocal], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          arrive_peer(peer_pv);
+          first = false;
+        }
+        ++n_seg;
+      }
+      if (issued) {
+        mma_commit(&bars[bDrain]);
+        mbar_wait(&bars[bDrain], 0, abort_flag, p.d_error, kWaitNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------
+    // Softmax warps: thread i <-> head i <-> TMEM lane i.
+    // ------------------------------------------------------------------
+    const int i = tid;
+    const bool owner = (i >> 6) == static_cast<int>(c);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + 128;
+    const int xrow_peer = i - 64 * static_cast<int>(peer);  // my row in the peer's X (shippers)
+    const int xrow_own = i - 64 * static_cast<int>(c);      // my row in my X (owners)
+    const uint32_t peer_x = peer_of(smem_u32(sX) + xrow_peer * 512, peer);
+    const uint32_t peer_p = peer_of(smem_u32(sP), peer);
+    const uint32_t peer_alpha = peer_of(smem_u32(sAlpha + (xrow_own & 63)), peer);
+    const uint32_t peer_stats = peer_of(smem_u32(sStats + (xrow_own & 63)), peer);
+    const uint32_t pb_xfull = peer_of(smem_u32(&bars[bXFull]), peer);
+    const uint32_t pb_xfree = peer_of(smem_u32(&bars[bXFree]), peer);
+    const uint32_t pb_pin = peer_of(smem_u32(&bars[bPIn]), peer);
+    const uint32_t pb_stats0 = peer_of(smem_u32(&bars[bStatsIn]), peer);
+    uint32_t n_tile = 0, n_seg = 0;
+    float m = -INFINITY, l = 0.f;
+    for (int64_t g = span.g_begin; g < span.g_end;) {
+      const int qidx = static_cast<int>(g / p.T);
+      const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
+      const int64_t seg_begin = g;
+      for (; g < seg_end; ++g, ++n_tile) {
+        const bool first = g == seg_begin;
+        mbar_wait(&bars[bSFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        __syncwarp();
+        tc_fence_after();
+        if (!owner) {
+          // Ship my row of the partial S to the peer (its owner's X).
+          if (n_tile > 0) mbar_wait_cluster(&bars[bXFree], (n_tile - 1) & 1, abort_flag, p.d_error);
+          __syncwarp();
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld32(tS + j * 32, r);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              st_peer_v4(peer_x + j * 128 + u * 16, r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+          }
+          arrive_peer(pb_xfull);
+          // The peer's owner of head i has written my P row and alpha.
+          mbar_wait_cluster(&bars[bPIn], n_tile & 1, abort_flag, p.d_error);
+          __syncwarp();
+          const float alpha = sAlpha[xrow_peer];
+          if (!first && alpha != 1.f) {
+#pragma unroll 1
+            for (int j = 0; j < 16; ++j) {
+              uint32_t o[16];
+              tmem_ld16(tO + j * 16, o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st16(tO + j * 16, o);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          mbar_arrive(&bars[bPFull]);
+        } else {
+          // Owner: S = my partial + the peer's, masked; running max; P.
+          const uint32_t mp = n_tile & 1;
+          mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+          const uint32_t mk0 = sMask[mp * 4 + 0], mk1 = sMask[mp * 4 + 1], mk2 = sMask[mp * 4 + 2],
+                         mk3 = sMask[mp * 4 + 3];
+          mbar_arrive(&bars[bMaskFree + mp]);
+          const uint32_t mk[4] = {mk0, mk1, mk2, mk3};
+          mbar_wait_cluster(&bars[bXFull], n_tile & 1, abort_flag, p.d_error);
+          __syncwarp();
+          const float* xr = sX + xrow_own * 128;
+          float mt = -INFINITY;
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld32(tS + j * 32, r);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int t = 32 * j + k;
+              const bool v = (mk[t & 3] >> (t >> 2)) & 1u;
+              const float x = (__uint_as_float(r[k]) + xr[t]) * p.scale_log2;
+              mt = v ? fmaxf(mt, x) : mt;
+            }
+          }
+          float alpha = 1.f;
+          if (mt > m + kLazy || (m == -INFINITY && mt > -INFINITY)) {
+            alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+            m = mt;
+          }
+          l *= alpha;
+          if (!first && alpha != 1.f) {
+#pragma unroll 1
+            for (int j = 0; j < 16; ++j) {
+              uint32_t o[16];
+              tmem_ld16(tO + j * 16, o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st16(tO + j * 16, o);
+            }
+            tmem_wait_st();
+          }
+          // Both CTAs' P operands are free once their PV of the previous tile is done.
+          if (n_tile > 0) mbar_wait_cluster(&bars[bPvPeer], (n_tile - 1) & 1, abort_flag, p.d_error);
+          __syncwarp();
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld32(tS + j * 32, r);
+            float pv[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int t = 32 * j + k;
+              const bool v = (mk[t & 3] >> (t >> 2)) & 1u;
+              const float x = (__uint_as_float(r[k]) + xr[t]) * p.scale_log2;
+              pv[k] = (v && m != -INFINITY) ? ex2_approx(x - m) : 0.f;
+              l += pv[k];
+            }
+            // 32 tokens = 4 units of 8 in P chunk j/2, units 4(j&1) .. +3.
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t off = (j >> 1) * 16384 + swz<128>(i * 128 + (4 * (j & 1) + u) * 16);
+              const uint32_t w0 = pack_bf16x2(pv[8 * u + 0], pv[8 * u + 1]);
+              const uint32_t w1 = pack_bf16x2(pv[8 * u + 2], pv[8 * u + 3]);
+              const uint32_t w2 = pack_bf16x2(pv[8 * u + 4], pv[8 * u + 5]);
+              const uint32_t w3 = pack_bf16x2(pv[8 * u + 6], pv[8 * u + 7]);
+              *reinterpret_cast<uint4*>(sP + off) = make_uint4(w0, w1, w2, w3);
+              st_peer_v4(peer_p + off, w0, w1, w2, w3);
+            }
+          }
+          arrive_peer(pb_xfree);  // done with my X row
+          st_peer_f32(peer_alpha, alpha);
+          fence_proxy_async_all();
+          arrive_peer(pb_pin);
+          tc_fence_before();
+          mbar_arrive(&bars[bPFull]);
+        }
+      }
+
+      // Epilogue of this query token (or split): O row i of my dim half / l.
+      const uint32_t sp = n_seg & 1;
+      float linv;
+      const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
+      const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
+      const int64_t split = static_cast<int64_t>(p.num_splits[qidx]) + local;
+      const bool direct = nsplit == 1;
+      const bool split_ok = direct || (split >= 0 && split < p.ws_splits_cap && local < nsplit);
+      if (owner) {
+        linv = l > 0.f ? 1.f / l : 0.f;
+        st_peer_f32(peer_stats + sp * 256, linv);
+        arrive_peer(pb_stats0 + sp * 8);
+        const float lse = l > 0.f ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
+        const int64_t hrow = static_cast<int64_t>(qidx) * p.h_q + i;
+        if (direct)
+          p.lse[hrow] = lse;
+        else if (split_ok)
+          p.ws_lse[split * p.h_q + i] = lse;
+        if (!split_ok && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_METADATA);
+        m = -INFINITY;
+        l = 0.f;
+      } else {
+        mbar_wait_cluster(&bars[bStatsIn + sp], (n_seg >> 1) & 1, abort_flag, p.d_error);
+        linv = sStats[sp * 64 + xrow_peer];
+      }
+      mbar_wait(&bars[bOReady], n_seg & 1, abort_flag, p.d_error, kWaitNs);
+      __syncwarp();
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(qidx) * p.h_q + i;
+#pragma unroll 1
+      for (int j = 0; j < 8; ++j) {
+        uint32_t o[32];
+        tmem_ld32(tO + j * 32, o);
+        const int d0 = static_cast<int>(c) * kHalf + j * 32;
+        if (direct) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * kD + d0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * u + 0]) * linv, __uint_as_float(o[8 * u + 1]) * linv),
+                                pack_bf16x2(__uint_as_float(o[8 * u + 2]) * linv, __uint_as_float(o[8 * u + 3]) * linv),
+                                pack_bf16x2(__uint_as_float(o[8 * u + 4]) * linv, __uint_as_float(o[8 * u + 5]) * linv),
+                                pack_bf16x2(__uint_as_float(o[8 * u + 6]) * linv, __uint_as_float(o[8 * u + 7]) * linv));
+        } else if (split_ok) {
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + (split * p.h_q + i) * kD + d0);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            dst[u] = make_float4(__uint_as_float(o[4 * u + 0]) * linv, __uint_as_float(o[4 * u + 1]) * linv,
+                                 __uint_as_float(o[4 * u + 2]) * linv, __uint_as_float(o[4 * u + 3]) * linv);
+        }
+      }
+      tc_fence_before();
+      ++n_seg;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer is done with this CTA's shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    tried = true;
+  }
+  return fn;
+}
+
+}  // namespace
+
+int decode_pair_smem_bytes() { return PairSmem::kAlloc; }
+
+cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_t stream) {
+  constexpr int smem = PairSmem::kAlloc;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap q_map, kv_map, scl_map;
+  {
+    // Q as [nq * 128 rows][512 bf16]; box: 128 heads x 64 dims, 128-byte swizzle.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.nq) * kHeads};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    const cuuint32_t box[2] = {64, kHeads};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // The FP8 pool as [tokens][528 bytes]; rows gathered 64 bytes (one 64-dim chunk) or 16 bytes (scales) at a time.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRecFp8), static_cast<cuuint64_t>(p.pool_tokens)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRecFp8)};
+    const cuuint32_t estr[2] = {1, 1};
+    const cuuint32_t box_d[2] = {64, 1};
+    const cuuint32_t box_s[2] = {16, 1};
+    if (enc(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.kv), dims, strides, box_d, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (enc(&scl_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.kv), dims, strides, box_s, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  sparse_decode_pair_kernel<<<2 * num_parts, kPThreads, smem, stream>>>(p, q_map, kv_map, scl_map);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

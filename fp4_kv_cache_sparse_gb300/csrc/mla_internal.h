@@ -44,6 +44,10 @@ template <int NH>
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);
 int decode_smem_bytes(int nh);
 
+// 128 heads, FP8 main cache only: a 2-CTA cluster per part splitting the latent dims.
+cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_t stream);
+int decode_pair_smem_bytes();
+
 cudaError_t launch_metadata(const Plan& plan, int nq, int32_t* d_sched, int32_t* d_num_splits, cudaStream_t stream);
 
 cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, const float* lse_part, uint16_t* out,
