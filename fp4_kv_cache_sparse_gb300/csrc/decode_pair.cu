@@ -20,10 +20,14 @@
 //     the rescale factor alpha of each of their heads; shippers apply the
 //     peer's alpha to their O rows.
 //   - 1/l at the end of a query token goes the same way.
-// Records reach shared memory by TMA row gathers (tile::gather4, 4 tokens per
-// instruction, 64 bytes of one record's dim chunk per row) into a 3-slot
-// staging ring, so the dequantizing warps never have global loads in flight
-// when they publish a chunk.
+// The partial-S rows and the P rows travel as bulk asynchronous copies between
+// the two CTAs' shared memory (completion on the receiver's mbarrier).  Q
+// lives in TMEM (the A operand of S = Q K^T), which leaves shared memory for a
+// double-buffered bf16 tile: the dequantizers fill the next tile while the
+// current one is in use.  Records reach shared memory by TMA row gathers
+// (tile::gather4, 4 tokens per instruction, 64 bytes of one record's dim chunk
+// per row) into a 3-slot staging ring, so the dequantizing warps never have
+// global loads in flight when they publish a chunk.
 //
 // Warps: 0-3 softmax (thread i <-> head i <-> TMEM lane i), 4-11 dequant,
 // 12 loader (indices, validity mask, all TMA), 13 tensor-core issuer.
@@ -46,18 +50,21 @@ constexpr int kLoaderWarp = 12;
 constexpr int kIssueWarp = 13;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLazy = 8.0f;
+constexpr uint32_t kXBytes = 64 * 512;          // 64 rows of 128 fp32 scores
+constexpr uint32_t kPInBytes = 2 * 8192 + 256;  // the peer's 64 P rows (2 chunks) + 64 alphas
 
 struct PairSmem {
-  static constexpr int kQ = 0;                   // 4 chunks x [128 heads x 128 B], SW128
-  static constexpr int kKV = kQ + 65536;         // 4 chunks x [128 tokens x 128 B], SW128
-  static constexpr int kP = kKV + 65536;         // 2 chunks x [128 heads x 128 B] (64 tokens each)
-  static constexpr int kX = kP + 32768;          // [64 heads][128 tokens] fp32 from the peer
+  static constexpr int kKV = 0;                  // 2 buffers x 4 chunks x [128 tokens x 128 B], SW128
+  static constexpr int kP = kKV + 2 * 65536;     // 2 chunks x [128 heads x 128 B] (64 tokens each); also
+                                                 // the outgoing staging of 64 rows of partial S
+  static constexpr int kX = kP + 32768;          // [64 rows][128 fp32] from the peer, 16-byte units swizzled
   static constexpr int kStg = kX + 32768;        // 3 slots x [128 tokens x 64 B] raw e4m3
   static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [32 groups x 128 B]: 4 tokens x 16 B scales
-  static constexpr int kBar = kScl + 2 * 4096;   // 40 mbarriers
-  static constexpr int kMask = kBar + 40 * 8;    // [2][4] u32 validity bits
-  static constexpr int kAlpha = kMask + 32;      // [64] f32, from the peer
-  static constexpr int kStats = kAlpha + 256;    // [2][64] f32 (1/l), from the peer
+  static constexpr int kBar = kScl + 2 * 4096;   // 48 mbarriers
+  static constexpr int kMask = kBar + 48 * 8;    // [2][4] u32 validity bits
+  static constexpr int kAlphaIn = kMask + 32;    // [64] f32 from the peer
+  static constexpr int kAlphaOut = kAlphaIn + 256;  // [2][64] f32 to the peer (by tile parity)
+  static constexpr int kStats = kAlphaOut + 512;    // [2][64] f32 (1/l) from the peer
   static constexpr int kScalar = kStats + 512;   // tmem slot, abort flag
   static constexpr int kEnd = kScalar + 64;
   static constexpr int kAlloc = kEnd + 1024;
@@ -65,9 +72,13 @@ struct PairSmem {
 
 enum PairBar {
   bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
-  bKvFull = 14, bKvFree = 18, bQFull = 20, bQFree = 21, bSFull = 22, bXFull = 23, bXFree = 24,
-  bPIn = 25, bPFull = 26, bPvLocal = 27, bPvPeer = 28, bOReady = 29, bStatsIn = 30, bDrain = 32
+  bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27, bXFull = 28, bXFree = 29,
+  bOutFree = 30, bPIn = 31, bPFull = 32, bPvLocal = 33, bPvPeer = 34, bOReady = 35, bStatsIn = 36 /* [2] */,
+  bDrain = 38
 };
+
+// TMEM columns: S [0, 128), O [128, 384), Q (bf16 pairs) [384, 512).
+constexpr uint32_t kColS = 0, kColO = 128, kColQ = 384;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -82,17 +93,23 @@ __device__ __forceinline__ uint32_t peer_of(uint32_t local, uint32_t peer) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(peer));
   return r;
 }
-__device__ __forceinline__ void st_peer_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
 __device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 __device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+// Bulk copy of this CTA's shared memory into the peer's, completing on the
+// peer's mbarrier (transaction bytes).
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst_peer, const void* src, uint32_t bytes, uint32_t bar_peer) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_peer),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar_peer)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Wait on a barrier that the peer CTA arrives on (cluster-scope acquire).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -130,13 +147,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
       "r"(bytes)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
 // Four rows (tokens) of a 2-D byte tensor, x bytes in, into consecutive rows of dst.
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
                                             uint64_t* bar) {
@@ -144,6 +154,18 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
       "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M rows (lanes) x K
+// columns of packed bf16 pairs.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -160,12 +182,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%"
+      "30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+// Byte offset of 16-byte unit u (0..31) of row r in a [rows][512 B] block
+// whose units are XOR-swizzled by the row, so that 32 consecutive rows read
+// at the same logical unit hit 32 different bank groups.
+__device__ __forceinline__ uint32_t xoff(int r, int u) { return r * 512 + ((u ^ (r & 31)) << 4); }
 
 struct PSpan {
   int64_t g_begin, g_end;
@@ -186,20 +224,20 @@ __device__ __forceinline__ PSpan pair_span(const DecodeParams& p, int part) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
-    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap q_map,
-                              const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap scl_map) {
+    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kv_map,
+                              const __grid_constant__ CUtensorMap scl_map) {
   using L = PairSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + L::kQ;
   uint8_t* sKV = smem + L::kKV;
   uint8_t* sP = smem + L::kP;
-  float* sX = reinterpret_cast<float*>(smem + L::kX);
+  uint8_t* sX = smem + L::kX;
   uint8_t* sStg = smem + L::kStg;
   uint8_t* sScl = smem + L::kScl;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + L::kMask);
-  float* sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
+  float* sAlphaIn = reinterpret_cast<float*>(smem + L::kAlphaIn);
+  float* sAlphaOut = reinterpret_cast<float*>(smem + L::kAlphaOut);
   float* sStats = reinterpret_cast<float*>(smem + L::kStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kScalar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kScalar + 4);
@@ -221,16 +259,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bars[bSclFree + i], kProdWarps);
       mbar_init(&bars[bMaskFull + i], 1);
       mbar_init(&bars[bMaskFree + i], 64);
-      mbar_init(&bars[bKvFree + i], 1);
       mbar_init(&bars[bStatsIn + i], 64);
+      for (int k = 0; k < 4; ++k) mbar_init(&bars[bKvFull + 4 * i + k], kProdWarps);
+      for (int h = 0; h < 2; ++h) mbar_init(&bars[bKvFree + 2 * i + h], 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[bKvFull + i], kProdWarps);
-    mbar_init(&bars[bQFull], 1);
-    mbar_init(&bars[bQFree], 1);
+    mbar_init(&bars[bQFull], 128);
     mbar_init(&bars[bSFull], 1);
-    mbar_init(&bars[bXFull], 64);
-    mbar_init(&bars[bXFree], 64);
-    mbar_init(&bars[bPIn], 64);
+    mbar_init(&bars[bXFull], 1);
+    mbar_init(&bars[bXFree], 1);
+    mbar_init(&bars[bOutFree], 1);
+    mbar_init(&bars[bPIn], 1);
     mbar_init(&bars[bPFull], 128);
     mbar_init(&bars[bPvLocal], 1);
     mbar_init(&bars[bPvPeer], 1);
@@ -252,11 +290,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 
   if (warp == kLoaderWarp) {
     // ------------------------------------------------------------------
-    // Loader: indices -> validity mask, TMA gathers of record halves, Q.
+    // Loader: indices -> validity mask, TMA gathers of record halves.
     // Lane l covers tokens 4l .. 4l+3 of a tile.
     // ------------------------------------------------------------------
-    uint32_t n_tile = 0, n_seg = 0, n_chunk = 0;
-    int64_t seg_end = span.g_begin;
+    uint32_t n_tile = 0, n_chunk = 0;
     auto raw_ids = [&](int64_t g, int32_t (&id)[4]) {
       const int qidx = static_cast<int>(g / p.T);
       const int t = static_cast<int>(g - static_cast<int64_t>(qidx) * p.T);
@@ -273,19 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
       int32_t nxt2[4] = {-1, -1, -1, -1};
       if (g + 2 < span.g_end) raw_ids(g + 2, nxt2);
-      if (g == seg_end) {
-        const int qidx = static_cast<int>(g / p.T);
-        seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-        if (lane == 0) {
-          if (n_seg > 0) mbar_wait(&bars[bQFree], (n_seg - 1) & 1, abort_flag, p.d_error, kWaitNs);
-          mbar_expect_tx(&bars[bQFull], kHeads * kHalf * 2);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tma_load_2d(sQ + k * 16384, &q_map, static_cast<int>(c) * kHalf + k * 64, qidx * kHeads, &bars[bQFull]);
-        }
-        ++n_seg;
-      }
-      // Validity; rows for the gathers (-1 = out of the tensor: zero fill).
+      // Validity; rows for the gathers (-1 = outside the tensor: zero fill).
       int32_t row[4];
       uint32_t vbits[4];
 #pragma unroll
@@ -327,24 +352,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------------
-    // Dequantizers: staging (raw e4m3 + e8m0) -> bf16 tile chunk.
-    // Lane L (0..255) handles items L and L + 256 of a chunk; item i is
-    // token i >> 2, 16-dim segment i & 3.
+    // Dequantizers: staging (raw e4m3 + e8m0) -> bf16 tile chunk, into the
+    // tile buffer of the tile's parity.  Lane L (0..255) handles items L and
+    // L + 256 of a chunk; item i is token i >> 2, 16-dim segment i & 3.
     // ------------------------------------------------------------------
     const int L = tid - 128;
     uint32_t n_tile = 0, n_chunk = 0;
     for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
       const uint32_t mp = n_tile & 1;
+      const uint32_t buf = n_tile & 1;
 #pragma unroll 1
       for (int k = 0; k < 4; ++k, ++n_chunk) {
         const uint32_t slot = n_chunk % kStgSlots, use = n_chunk / kStgSlots;
         if (k == 0) mbar_wait(&bars[bSclFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
         mbar_wait(&bars[bStgFull + slot], use & 1, abort_flag, p.d_error, kWaitNs);
-        if ((k & 1) == 0 && n_tile > 0)
-          mbar_wait(&bars[bKvFree + (k >> 1)], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitNs);
+        if ((k & 1) == 0 && n_tile >= 2)
+          mbar_wait(&bars[bKvFree + 2 * buf + (k >> 1)], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
         const uint8_t* stg = sStg + slot * 8192;
         const uint8_t* scl = sScl + mp * 4096;
-        uint8_t* chunk = sKV + k * 16384;
+        uint8_t* chunk = sKV + buf * 65536 + k * 16384;
         uint4 raw[2];
         uint32_t sb[2];
         bool big = false;
@@ -372,7 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bars[bKvFull + k]);
+          mbar_arrive(&bars[bKvFull + 4 * buf + k]);
           mbar_arrive(&bars[bStgFree + slot]);
           if (k == 3) mbar_arrive(&bars[bSclFree + mp]);
         }
@@ -380,50 +406,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
   } else if (warp == kIssueWarp) {
     // ------------------------------------------------------------------
-    // Tensor-core issue (one thread).
+    // Tensor-core issue (one thread): S = Q K^T (A = Q in TMEM), then per
+    // tile O += P V followed at once by the next tile's S.
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
-      const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
-      const uint32_t tS = tmem, tO = tmem + 128;
+      const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
       const uint32_t peer_pv = peer_of(smem_u32(&bars[bPvPeer]), peer);
       uint32_t n_tile = 0, n_seg = 0;
       bool issued = false;
+      auto issue_qk = [&](uint32_t nt) {
+        const uint32_t buf = nt & 1;
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          mbar_wait(&bars[bKvFull + 4 * buf + k], (nt >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t b = make_smem_desc(kv_base + buf * 65536 + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
+            mma_bf16_ts(tS, tQ + k * 32 + kk * 8, b, idesc_qk, (k | kk) != 0);
+          }
+        }
+        mma_commit(&bars[bSFull]);
+      };
       for (int64_t g = span.g_begin; g < span.g_end;) {
         const int qidx = static_cast<int>(g / p.T);
         const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-        mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
         bool first = true;
         for (; g < seg_end; ++g, ++n_tile) {
-#pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
-            mbar_wait(&bars[bKvFull + k], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          if (first) {
+            // Q of this query token is in TMEM once the softmax warps have
+            // written it (after the previous token's epilogue).
+            mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = make_smem_desc(q_base + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
-              const uint64_t b = make_smem_desc(kv_base + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
-              mma_bf16_ss(tS, a, b, idesc_qk, (k | kk) != 0);
-            }
+            issue_qk(n_tile);
+            issued = true;
           }
-          issued = true;
-          mma_commit(&bars[bSFull]);
-          if (g + 1 == seg_end) mma_commit(&bars[bQFree]);
           mbar_wait(&bars[bPFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
           tc_fence_after();
+          const uint32_t buf = n_tile & 1;
 #pragma unroll 1
           for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint64_t a = make_smem_desc(p_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128);
-              const uint64_t b = make_smem_desc(kv_base + 2 * hh * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
+              const uint64_t b =
+                  make_smem_desc(kv_base + buf * 65536 + 2 * hh * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
               mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(first && ks == 0));
             }
-            mma_commit(&bars[bKvFree + hh]);
+            mma_commit(&bars[bKvFree + 2 * buf + hh]);
           }
           mma_commit(&bars[bPvLocal]);
           if (g + 1 == seg_end) mma_commit(&bars[bOReady]);
+          // The next tile of the same query token: its S right behind this PV.
+          if (g + 1 < seg_end) issue_qk(n_tile + 1);
           // Tell the peer that this CTA's P operand is free again.
           mbar_wait(&bars[bPvLocal], n_tile & 1, abort_flag, p.d_error, kWaitNs);
           arrive_peer(peer_pv);
@@ -443,54 +481,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------------------
     const int i = tid;
     const bool owner = (i >> 6) == static_cast<int>(c);
+    const int r = i & 63;  // my row in X / alpha / stats (mine as owner, the peer's as shipper)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + 128;
-    const int xrow_peer = i - 64 * static_cast<int>(peer);  // my row in the peer's X (shippers)
-    const int xrow_own = i - 64 * static_cast<int>(c);      // my row in my X (owners)
-    const uint32_t peer_x = peer_of(smem_u32(sX) + xrow_peer * 512, peer);
+    const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO, tQ = tmem + lane_base + kColQ;
+    const uint32_t peer_x = peer_of(smem_u32(sX), peer);
     const uint32_t peer_p = peer_of(smem_u32(sP), peer);
-    const uint32_t peer_alpha = peer_of(smem_u32(sAlpha + (xrow_own & 63)), peer);
-    const uint32_t peer_stats = peer_of(smem_u32(sStats + (xrow_own & 63)), peer);
+    const uint32_t peer_alpha = peer_of(smem_u32(sAlphaIn), peer);
+    const uint32_t peer_stats = peer_of(smem_u32(sStats + r), peer);
     const uint32_t pb_xfull = peer_of(smem_u32(&bars[bXFull]), peer);
     const uint32_t pb_xfree = peer_of(smem_u32(&bars[bXFree]), peer);
     const uint32_t pb_pin = peer_of(smem_u32(&bars[bPIn]), peer);
     const uint32_t pb_stats0 = peer_of(smem_u32(&bars[bStatsIn]), peer);
+    const uint32_t named = owner ? 2u : 3u;  // 64-thread barrier of my role
     uint32_t n_tile = 0, n_seg = 0;
     float m = -INFINITY, l = 0.f;
     for (int64_t g = span.g_begin; g < span.g_end;) {
       const int qidx = static_cast<int>(g / p.T);
       const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
       const int64_t seg_begin = g;
+      {
+        // Q row i, my half of the dims, into TMEM as packed bf16 pairs.
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qidx) * kHeads + i) * kD +
+                                                          static_cast<int>(c) * kHalf);
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = __ldg(src + j * 8 + u);
+            v[4 * u] = w.x;
+            v[4 * u + 1] = w.y;
+            v[4 * u + 2] = w.z;
+            v[4 * u + 3] = w.w;
+          }
+          tmem_st32(tQ + j * 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[bQFull]);
+      }
       for (; g < seg_end; ++g, ++n_tile) {
         const bool first = g == seg_begin;
         mbar_wait(&bars[bSFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
         __syncwarp();
         tc_fence_after();
         if (!owner) {
-          // Ship my row of the partial S to the peer (its owner's X).
-          if (n_tile > 0) mbar_wait_cluster(&bars[bXFree], (n_tile - 1) & 1, abort_flag, p.d_error);
-          __syncwarp();
+          // Shipper: my row of the partial S -> staging (in my P operand,
+          // free until my owners write P) -> one bulk copy to the peer's X.
+          if (r == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
-            uint32_t r[32];
-            tmem_ld32(tS + j * 32, r);
+            uint32_t v[32];
+            tmem_ld32(tS + j * 32, v);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-              st_peer_v4(peer_x + j * 128 + u * 16, r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+              *reinterpret_cast<uint4*>(sP + xoff(r, 8 * j + u)) =
+                  make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
           }
-          arrive_peer(pb_xfull);
-          // The peer's owner of head i has written my P row and alpha.
-          mbar_wait_cluster(&bars[bPIn], n_tile & 1, abort_flag, p.d_error);
+          fence_proxy_async_smem();
+          named_bar_sync(named, 64);
+          if (r == 0) {
+            if (n_tile > 0) mbar_wait_cluster(&bars[bXFree], (n_tile - 1) & 1, abort_flag, p.d_error);
+            bulk_to_peer(peer_x, sP, kXBytes, pb_xfull);
+            bulk_commit_and_wait_read();
+            mbar_arrive(&bars[bOutFree]);
+          }
+          // The peer's owners' P rows for my heads and their alphas.
+          mbar_wait(&bars[bPIn], n_tile & 1, abort_flag, p.d_error, kWaitNs);
           __syncwarp();
-          const float alpha = sAlpha[xrow_peer];
+          const float alpha = sAlphaIn[r];
           if (!first && alpha != 1.f) {
 #pragma unroll 1
-            for (int j = 0; j < 16; ++j) {
-              uint32_t o[16];
-              tmem_ld16(tO + j * 16, o);
+            for (int j = 0; j < 8; ++j) {
+              uint32_t o[32];
+              tmem_ld32(tO + j * 32, o);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st16(tO + j * 16, o);
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(tO + j * 32, o);
             }
             tmem_wait_st();
           }
@@ -498,26 +565,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           mbar_arrive(&bars[bPFull]);
         } else {
           // Owner: S = my partial + the peer's, masked; running max; P.
+          if (r == 0) mbar_expect_tx(&bars[bXFull], kXBytes);
           const uint32_t mp = n_tile & 1;
           mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          const uint32_t mk0 = sMask[mp * 4 + 0], mk1 = sMask[mp * 4 + 1], mk2 = sMask[mp * 4 + 2],
-                         mk3 = sMask[mp * 4 + 3];
+          uint32_t mk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mk[j] = sMask[mp * 4 + j];
           mbar_arrive(&bars[bMaskFree + mp]);
-          const uint32_t mk[4] = {mk0, mk1, mk2, mk3};
-          mbar_wait_cluster(&bars[bXFull], n_tile & 1, abort_flag, p.d_error);
+          mbar_wait(&bars[bXFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
           __syncwarp();
-          const float* xr = sX + xrow_own * 128;
           float mt = -INFINITY;
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
-            uint32_t r[32];
-            tmem_ld32(tS + j * 32, r);
+            uint32_t v[32];
+            tmem_ld32(tS + j * 32, v);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int t = 32 * j + k;
-              const bool v = (mk[t & 3] >> (t >> 2)) & 1u;
-              const float x = (__uint_as_float(r[k]) + xr[t]) * p.scale_log2;
-              mt = v ? fmaxf(mt, x) : mt;
+            for (int u = 0; u < 8; ++u) {
+              const float4 x4 = *reinterpret_cast<const float4*>(sX + xoff(r, 8 * j + u));
+              const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int t = 32 * j + 4 * u + e;
+                const bool ok = (mk[e] >> (t >> 2)) & 1u;  // t & 3 == e
+                const float x = (__uint_as_float(v[4 * u + e]) + xs[e]) * p.scale_log2;
+                mt = ok ? fmaxf(mt, x) : mt;
+              }
             }
           }
           float alpha = 1.f;
@@ -528,47 +600,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           l *= alpha;
           if (!first && alpha != 1.f) {
 #pragma unroll 1
-            for (int j = 0; j < 16; ++j) {
-              uint32_t o[16];
-              tmem_ld16(tO + j * 16, o);
+            for (int j = 0; j < 8; ++j) {
+              uint32_t o[32];
+              tmem_ld32(tO + j * 32, o);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st16(tO + j * 16, o);
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(tO + j * 32, o);
             }
             tmem_wait_st();
           }
-          // Both CTAs' P operands are free once their PV of the previous tile is done.
-          if (n_tile > 0) mbar_wait_cluster(&bars[bPvPeer], (n_tile - 1) & 1, abort_flag, p.d_error);
+          // My P operand still holds the outgoing S until the shippers'
+          // copy has read it.
+          mbar_wait(&bars[bOutFree], n_tile & 1, abort_flag, p.d_error, kWaitNs);
           __syncwarp();
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
-            uint32_t r[32];
-            tmem_ld32(tS + j * 32, r);
+            uint32_t v[32];
+            tmem_ld32(tS + j * 32, v);
             float pv[32];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int t = 32 * j + k;
-              const bool v = (mk[t & 3] >> (t >> 2)) & 1u;
-              const float x = (__uint_as_float(r[k]) + xr[t]) * p.scale_log2;
-              pv[k] = (v && m != -INFINITY) ? ex2_approx(x - m) : 0.f;
-              l += pv[k];
+            for (int u = 0; u < 8; ++u) {
+              const float4 x4 = *reinterpret_cast<const float4*>(sX + xoff(r, 8 * j + u));
+              const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int t = 32 * j + 4 * u + e;
+                const bool ok = (mk[e] >> (t >> 2)) & 1u;
+                const float x = (__uint_as_float(v[4 * u + e]) + xs[e]) * p.scale_log2;
+                const float pe = (ok && m != -INFINITY) ? ex2_approx(x - m) : 0.f;
+                pv[4 * u + e] = pe;
+                l += pe;
+              }
             }
             // 32 tokens = 4 units of 8 in P chunk j/2, units 4(j&1) .. +3.
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const uint32_t off = (j >> 1) * 16384 + swz<128>(i * 128 + (4 * (j & 1) + u) * 16);
-              const uint32_t w0 = pack_bf16x2(pv[8 * u + 0], pv[8 * u + 1]);
-              const uint32_t w1 = pack_bf16x2(pv[8 * u + 2], pv[8 * u + 3]);
-              const uint32_t w2 = pack_bf16x2(pv[8 * u + 4], pv[8 * u + 5]);
-              const uint32_t w3 = pack_bf16x2(pv[8 * u + 6], pv[8 * u + 7]);
-              *reinterpret_cast<uint4*>(sP + off) = make_uint4(w0, w1, w2, w3);
-              st_peer_v4(peer_p + off, w0, w1, w2, w3);
+              *reinterpret_cast<uint4*>(sP + off) =
+                  make_uint4(pack_bf16x2(pv[8 * u + 0], pv[8 * u + 1]), pack_bf16x2(pv[8 * u + 2], pv[8 * u + 3]),
+                             pack_bf16x2(pv[8 * u + 4], pv[8 * u + 5]), pack_bf16x2(pv[8 * u + 6], pv[8 * u + 7]));
             }
           }
-          arrive_peer(pb_xfree);  // done with my X row
-          st_peer_f32(peer_alpha, alpha);
-          fence_proxy_async_all();
-          arrive_peer(pb_pin);
+          float* alpha_out = sAlphaOut + (n_tile & 1) * 64;
+          alpha_out[r] = alpha;
+          fence_proxy_async_smem();
+          named_bar_sync(named, 64);
+          if (r == 0) {
+            arrive_peer(pb_xfree);  // my X rows are read
+            // The peer's P operand is free once its PV of the previous tile is done.
+            if (n_tile > 0) mbar_wait_cluster(&bars[bPvPeer], (n_tile - 1) & 1, abort_flag, p.d_error);
+            const uint32_t rows = static_cast<uint32_t>(c) * 64 * 128;  // my 64 rows of each P chunk
+            bulk_to_peer(peer_p + rows, sP + rows, 8192, pb_pin);
+            bulk_to_peer(peer_p + 16384 + rows, sP + 16384 + rows, 8192, pb_pin);
+            bulk_to_peer(peer_alpha, alpha_out, 256, pb_pin);
+            bulk_commit_and_wait_read();
+          }
           tc_fence_before();
           mbar_arrive(&bars[bPFull]);
         }
@@ -597,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         l = 0.f;
       } else {
         mbar_wait_cluster(&bars[bStatsIn + sp], (n_seg >> 1) & 1, abort_flag, p.d_error);
-        linv = sStats[sp * 64 + xrow_peer];
+        linv = sStats[sp * 64 + r];
       }
       mbar_wait(&bars[bOReady], n_seg & 1, abort_flag, p.d_error, kWaitNs);
       __syncwarp();
@@ -671,18 +757,7 @@ cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap q_map, kv_map, scl_map;
-  {
-    // Q as [nq * 128 rows][512 bf16]; box: 128 heads x 64 dims, 128-byte swizzle.
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.nq) * kHeads};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
-    const cuuint32_t box[2] = {64, kHeads};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  CUtensorMap kv_map, scl_map;
   {
     // The FP8 pool as [tokens][528 bytes]; rows gathered 64 bytes (one 64-dim chunk) or 16 bytes (scales) at a time.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRecFp8), static_cast<cuuint64_t>(p.pool_tokens)};
@@ -699,7 +774,7 @@ cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  sparse_decode_pair_kernel<<<2 * num_parts, kPThreads, smem, stream>>>(p, q_map, kv_map, scl_map);
+  sparse_decode_pair_kernel<<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map, scl_map);
   return cudaGetLastError();
 }
 
