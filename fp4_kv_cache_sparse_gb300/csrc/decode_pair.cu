@@ -6,28 +6,23 @@
 // "Arithmetic intensity" and "Workarounds"; "deepseek-ai/FlashMLA", "How to use
 // it"), for an FP8 main cache without an extra cache.  The layout differs:
 // heads are the MMA's M dimension (all 128 of them), so both products run on
-// the tensor core at full rate -- S = Q K^T with N = 128 tokens and
-// O = P V with N = 128 dims per instruction -- instead of the 64-head,
+// the tensor core with N = 128 per instruction instead of the 64-head,
 // tokens-on-M form whose small N leaves the tensor core waiting on shared
 // memory.  O for 128 heads x 512 dims would fill all of TMEM, so CTA c of the
-// pair owns dims [256c, 256c + 256): its half of every record, of Q, of the
-// bf16 tile and of O.  Each CTA's S is a partial sum over its half; the halves
-// are exchanged through distributed shared memory:
-//   - S: CTA c owns the softmax of heads [64c, 64c + 64); the two warps whose
-//     TMEM lanes hold the other 64 heads ship those rows of the partial S to
-//     the peer ("shippers"), the owners add the peer's rows to their own.
-//   - P: owners write their rows of P (bf16) into both CTAs' P operand, plus
-//     the rescale factor alpha of each of their heads; shippers apply the
-//     peer's alpha to their O rows.
-//   - 1/l at the end of a query token goes the same way.
-// The partial-S rows and the P rows travel as bulk asynchronous copies between
-// the two CTAs' shared memory (completion on the receiver's mbarrier).  Q
-// lives in TMEM (the A operand of S = Q K^T), which leaves shared memory for a
-// double-buffered bf16 tile: the dequantizers fill the next tile while the
-// current one is in use.  Records reach shared memory by TMA row gathers
-// (tile::gather4, 4 tokens per instruction, 64 bytes of one record's dim chunk
-// per row) into a 3-slot staging ring, so the dequantizing warps never have
-// global loads in flight when they publish a chunk.
+// pair owns dims [256c, 256c + 256): its half of every record, of Q (kept in
+// TMEM as the A operand of S = Q K^T), of the bf16 tile and of O.  Each CTA's
+// S is a partial sum over its dims; CTA c computes the softmax of token half
+// c of every tile for all heads: it sends the peer its partial scores of the
+// other token half and receives the peer's for its own half (bulk
+// asynchronous copies between the two shared memories, completing on the
+// receiver's mbarrier), the two CTAs swap per-head tile maxima so that they
+// keep identical running maxima (and rescale factors), and each sends the
+// other its half of P, so both hold all of P for their PV.  Q in TMEM leaves
+// shared memory for a double-buffered bf16 tile: the dequantizers fill the
+// next tile while the current one is in use.  Records reach shared memory by
+// TMA row gathers (tile::gather4, 4 tokens per instruction, 64 bytes of one
+// record's dim chunk per row) into a 3-slot staging ring, so the dequantizing
+// warps never have global loads in flight when they publish a chunk.
 //
 // Warps: 0-3 softmax (thread i <-> head i <-> TMEM lane i), 4-11 dequant,
 // 12 loader (indices, validity mask, all TMA), 13 tensor-core issuer.
@@ -50,31 +45,32 @@ constexpr int kLoaderWarp = 12;
 constexpr int kIssueWarp = 13;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLazy = 8.0f;
-constexpr uint32_t kXBytes = 64 * 512;          // 64 rows of 128 fp32 scores
-constexpr uint32_t kPInBytes = 2 * 8192 + 256;  // the peer's 64 P rows (2 chunks) + 64 alphas
+constexpr uint32_t kXBytes = 128 * 256;         // 128 heads x 64 tokens of fp32 scores (the other CTA's half)
+constexpr uint32_t kPInBytes = 16384;           // the peer's P chunk: 128 heads x 64 tokens bf16
 
 struct PairSmem {
   static constexpr int kKV = 0;                  // 2 buffers x 4 chunks x [128 tokens x 128 B], SW128
   static constexpr int kP = kKV + 2 * 65536;     // 2 chunks x [128 heads x 128 B] (64 tokens each); also
-                                                 // the outgoing staging of 64 rows of partial S
-  static constexpr int kX = kP + 32768;          // [64 rows][128 fp32] from the peer, 16-byte units swizzled
-  static constexpr int kStg = kX + 32768;        // 3 slots x [128 tokens x 64 B] raw e4m3
-  static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [32 groups x 128 B]: 4 tokens x 16 B scales
-  static constexpr int kBar = kScl + 2 * 4096;   // 48 mbarriers
+                                                 // the outgoing staging of the partial scores
+  static constexpr int kX = kP + 32768;          // [128 heads][64 tokens] fp32 from the peer, units swizzled
+  static constexpr int kStg = kX + 32768;        // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
+  static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [128 tokens x 8 B] e8m0 scales of this CTA's dims
+  static constexpr int kBar = kScl + 2 * 1024;   // 48 mbarriers
   static constexpr int kMask = kBar + 48 * 8;    // [2][4] u32 validity bits
-  static constexpr int kAlphaIn = kMask + 32;    // [64] f32 from the peer
-  static constexpr int kAlphaOut = kAlphaIn + 256;  // [2][64] f32 to the peer (by tile parity)
-  static constexpr int kStats = kAlphaOut + 512;    // [2][64] f32 (1/l) from the peer
-  static constexpr int kScalar = kStats + 512;   // tmem slot, abort flag
-  static constexpr int kEnd = kScalar + 64;
+  static constexpr int kMaxIn = kMask + 32;      // [128] f32 tile maxima from the peer
+  static constexpr int kMaxOut = kMaxIn + 512;   // [128] f32 tile maxima for the peer
+  static constexpr int kStats = kMaxOut + 512;   // [2][128] f32 row sums from the peer
+  static constexpr int kStatsOut = kStats + 1024;  // [128] f32 row sums for the peer
+  static constexpr int kScalar = kStatsOut + 512;  // tmem slot, abort flag
+  static constexpr int kEnd = kScalar + 16;
   static constexpr int kAlloc = kEnd + 1024;
 };
 
 enum PairBar {
   bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
-  bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27, bXFull = 28, bXFree = 29,
-  bOutFree = 30, bPIn = 31, bPFull = 32, bPvLocal = 33, bPvPeer = 34, bOReady = 35, bStatsIn = 36 /* [2] */,
-  bDrain = 38
+  bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27, bXFull = 28,
+  bOutFree = 30, bPIn = 31, bPFull = 32, bOReady = 35, bStatsIn = 36 /* [2] */,
+  bMaxFull = 38, bDrain = 39
 };
 
 // TMEM columns: S [0, 128), O [128, 384), Q (bf16 pairs) [384, 512).
@@ -93,12 +89,6 @@ __device__ __forceinline__ uint32_t peer_of(uint32_t local, uint32_t peer) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(peer));
   return r;
 }
-__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void arrive_peer(uint32_t bar_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
-}
 // Bulk copy of this CTA's shared memory into the peer's, completing on the
 // peer's mbarrier (transaction bytes).
 __device__ __forceinline__ void bulk_to_peer(uint32_t dst_peer, const void* src, uint32_t bytes, uint32_t bar_peer) {
@@ -109,35 +99,6 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_peer, const void* src,
 }
 __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait on a barrier that the peer CTA arrives on (cluster-scope acquire).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  int32_t* d_error) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitNs) {
-        *abort_flag = 1;
-        if (d_error) atomicOr(d_error, MLA_DEVERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -200,10 +161,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// Byte offset of 16-byte unit u (0..31) of row r in a [rows][512 B] block
-// whose units are XOR-swizzled by the row, so that 32 consecutive rows read
-// at the same logical unit hit 32 different bank groups.
-__device__ __forceinline__ uint32_t xoff(int r, int u) { return r * 512 + ((u ^ (r & 31)) << 4); }
+// Byte offset of 16-byte unit u (0..15) of row r in a [rows][256 B] block
+// whose units are XOR-swizzled by the row, so that consecutive rows read at
+// the same logical unit spread over the bank groups.
+__device__ __forceinline__ uint32_t xoff(int r, int u) { return r * 256 + ((u ^ (r & 15)) << 4); }
 
 struct PSpan {
   int64_t g_begin, g_end;
@@ -224,8 +185,7 @@ __device__ __forceinline__ PSpan pair_span(const DecodeParams& p, int part) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
-    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kv_map,
-                              const __grid_constant__ CUtensorMap scl_map) {
+    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kv_map) {
   using L = PairSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -236,9 +196,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   uint8_t* sScl = smem + L::kScl;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + L::kMask);
-  float* sAlphaIn = reinterpret_cast<float*>(smem + L::kAlphaIn);
-  float* sAlphaOut = reinterpret_cast<float*>(smem + L::kAlphaOut);
+  float* sMaxIn = reinterpret_cast<float*>(smem + L::kMaxIn);
+  float* sMaxOut = reinterpret_cast<float*>(smem + L::kMaxOut);
   float* sStats = reinterpret_cast<float*>(smem + L::kStats);
+  float* sStatsOut = reinterpret_cast<float*>(smem + L::kStatsOut);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kScalar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kScalar + 4);
 
@@ -258,21 +219,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bars[bSclFull + i], 1);
       mbar_init(&bars[bSclFree + i], kProdWarps);
       mbar_init(&bars[bMaskFull + i], 1);
-      mbar_init(&bars[bMaskFree + i], 64);
-      mbar_init(&bars[bStatsIn + i], 64);
+      mbar_init(&bars[bMaskFree + i], 128);
+      mbar_init(&bars[bStatsIn + i], 1);
       for (int k = 0; k < 4; ++k) mbar_init(&bars[bKvFull + 4 * i + k], kProdWarps);
       for (int h = 0; h < 2; ++h) mbar_init(&bars[bKvFree + 2 * i + h], 1);
     }
     mbar_init(&bars[bQFull], 128);
     mbar_init(&bars[bSFull], 1);
     mbar_init(&bars[bXFull], 1);
-    mbar_init(&bars[bXFree], 1);
     mbar_init(&bars[bOutFree], 1);
     mbar_init(&bars[bPIn], 1);
     mbar_init(&bars[bPFull], 128);
-    mbar_init(&bars[bPvLocal], 1);
-    mbar_init(&bars[bPvPeer], 1);
     mbar_init(&bars[bOReady], 1);
+    mbar_init(&bars[bMaxFull], 1);
     mbar_init(&bars[bDrain], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -290,7 +249,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 
   if (warp == kLoaderWarp) {
     // ------------------------------------------------------------------
-    // Loader: indices -> validity mask, TMA gathers of record halves.
+    // Loader: indices -> validity mask; this CTA's 8 scale bytes of every
+    // record by plain loads, one tile ahead; TMA row gathers of the record
+    // halves (256 bytes per token), 32 tokens per staging slot.
     // Lane l covers tokens 4l .. 4l+3 of a tile.
     // ------------------------------------------------------------------
     uint32_t n_tile = 0, n_chunk = 0;
@@ -304,35 +265,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         id[j] = slot < p.topk ? __ldg(ids + slot) : -1;
       }
     };
+    auto valid_id = [&](int32_t id) { return id >= 0 && static_cast<int64_t>(id) < p.pool_tokens; };
+    auto load_scales = [&](const int32_t (&id)[4], uint2 (&sc)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        sc[j] = valid_id(id[j]) ? __ldg(reinterpret_cast<const uint2*>(p.kv + static_cast<int64_t>(id[j]) * kRecFp8 +
+                                                                      kD + 8 * c))
+                                : make_uint2(0u, 0u);
+    };
     int32_t cur[4] = {-1, -1, -1, -1}, nxt[4] = {-1, -1, -1, -1};
+    uint2 sc_cur[4] = {}, sc_nxt[4] = {};
     if (span.g_begin < span.g_end) raw_ids(span.g_begin, cur);
     if (span.g_begin + 1 < span.g_end) raw_ids(span.g_begin + 1, nxt);
+    load_scales(cur, sc_cur);
     for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
-      int32_t nxt2[4] = {-1, -1, -1, -1};
-      if (g + 2 < span.g_end) raw_ids(g + 2, nxt2);
       // Validity; rows for the gathers (-1 = outside the tensor: zero fill).
       int32_t row[4];
       uint32_t vbits[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int32_t id = cur[j];
-        const bool valid = id >= 0 && static_cast<int64_t>(id) < p.pool_tokens;
+        const bool valid = valid_id(id);
         if (!valid && id != -1 && c == 0 && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_INDEX);
         row[j] = valid ? id : -1;
         vbits[j] = __ballot_sync(0xFFFFFFFFu, valid);
       }
       const uint32_t mp = n_tile & 1;
+      if (n_tile >= 2) mbar_wait(&bars[bSclFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint2*>(sScl + mp * 1024 + (4 * lane + j) * 8) = sc_cur[j];
+      __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&bars[bSclFull + mp]);
         if (n_tile >= 2) mbar_wait(&bars[bMaskFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
 #pragma unroll
         for (int j = 0; j < 4; ++j) sMask[mp * 4 + j] = vbits[j];
         mbar_arrive(&bars[bMaskFull + mp]);
-        if (n_tile >= 2) mbar_wait(&bars[bSclFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
-        mbar_expect_tx(&bars[bSclFull + mp], 32 * 64);
       }
-      __syncwarp();
-      tma_gather4(sScl + mp * 4096 + lane * 128, &scl_map, 512, row[0], row[1], row[2], row[3],
-                  &bars[bSclFull + mp]);
 #pragma unroll 1
       for (int k = 0; k < 4; ++k, ++n_chunk) {
         const uint32_t slot = n_chunk % kStgSlots, use = n_chunk / kStgSlots;
@@ -341,20 +311,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           mbar_expect_tx(&bars[bStgFull + slot], 32 * 256);
         }
         __syncwarp();
-        tma_gather4(sStg + slot * 8192 + lane * 256, &kv_map, static_cast<int>(c) * kHalf + k * 64, row[0], row[1],
-                    row[2], row[3], &bars[bStgFull + slot]);
+        if ((lane >> 3) == k)
+          tma_gather4(sStg + slot * 8192 + (lane & 7) * 1024, &kv_map, static_cast<int>(c) * kHalf, row[0], row[1],
+                      row[2], row[3], &bars[bStgFull + slot]);
       }
+      // Next tile's scales and the indices of the tile after it, issued only
+      // now so that no load is in flight at this tile's arrivals.
+      load_scales(nxt, sc_nxt);
+      int32_t nxt2[4] = {-1, -1, -1, -1};
+      if (g + 2 < span.g_end) raw_ids(g + 2, nxt2);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         cur[j] = nxt[j];
         nxt[j] = nxt2[j];
+        sc_cur[j] = sc_nxt[j];
       }
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------------
-    // Dequantizers: staging (raw e4m3 + e8m0) -> bf16 tile chunk, into the
-    // tile buffer of the tile's parity.  Lane L (0..255) handles items L and
-    // L + 256 of a chunk; item i is token i >> 2, 16-dim segment i & 3.
+    // Dequantizers: staging slot (32 tokens x this CTA's 256 dims, raw e4m3)
+    // + scales -> bf16 tile rows, into the tile buffer of the tile's parity.
+    // Lane L (0..255) handles items L and L + 256 of a slot; item i is token
+    // i >> 4, 16-dim segment i & 15.
     // ------------------------------------------------------------------
     const int L = tid - 128;
     uint32_t n_tile = 0, n_chunk = 0;
@@ -364,36 +342,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll 1
       for (int k = 0; k < 4; ++k, ++n_chunk) {
         const uint32_t slot = n_chunk % kStgSlots, use = n_chunk / kStgSlots;
-        if (k == 0) mbar_wait(&bars[bSclFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+        if (k == 0) {
+          mbar_wait(&bars[bSclFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+          if (n_tile >= 2) {
+            mbar_wait(&bars[bKvFree + 2 * buf], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
+            mbar_wait(&bars[bKvFree + 2 * buf + 1], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
+          }
+        }
         mbar_wait(&bars[bStgFull + slot], use & 1, abort_flag, p.d_error, kWaitNs);
-        if ((k & 1) == 0 && n_tile >= 2)
-          mbar_wait(&bars[bKvFree + 2 * buf + (k >> 1)], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
         const uint8_t* stg = sStg + slot * 8192;
-        const uint8_t* scl = sScl + mp * 4096;
-        uint8_t* chunk = sKV + buf * 65536 + k * 16384;
+        const uint8_t* scl = sScl + mp * 1024;
+        uint8_t* tile = sKV + buf * 65536;
         uint4 raw[2];
         uint32_t sb[2];
         bool big = false;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int item = L + 256 * r;
-          const int t = item >> 2, s = item & 3;
-          raw[r] = *reinterpret_cast<const uint4*>(stg + t * 64 + s * 16);
-          sb[r] = scl[(t >> 2) * 128 + (t & 3) * 16 + c * 8 + k * 2 + (s >> 1)];
+          const int tt = item >> 4, s = item & 15;
+          raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
+          sb[r] = scl[(32 * k + tt) * 8 + (s >> 1)];
           big |= sb[r] > 142u;
         }
         const bool any_big = __any_sync(0xFFFFFFFFu, big);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int item = L + 256 * r;
-          const int t = item >> 2, s = item & 3;
+          const int t = 32 * k + (item >> 4), s = item & 15;
           uint32_t o[8];
           if (!any_big)
             dequant_fp8_16_small_scale(raw[r], sb[r], o);
           else
             dequant_fp8_16(raw[r], sb[r], o);
-          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (2 * s) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (2 * s + 1) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+          uint8_t* chunk = tile + (s >> 2) * 16384;
+          const int u = 2 * (s & 3);
+          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + u * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + 1) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -414,15 +398,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
       const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
       const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
-      const uint32_t peer_pv = peer_of(smem_u32(&bars[bPvPeer]), peer);
       uint32_t n_tile = 0, n_seg = 0;
       bool issued = false;
       auto issue_qk = [&](uint32_t nt) {
         const uint32_t buf = nt & 1;
 #pragma unroll 1
+        for (int k = 0; k < 4; ++k) mbar_wait(&bars[bKvFull + 4 * buf + k], (nt >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+        tc_fence_after();
+#pragma unroll 1
         for (int k = 0; k < 4; ++k) {
-          mbar_wait(&bars[bKvFull + 4 * buf + k], (nt >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t b = make_smem_desc(kv_base + buf * 65536 + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
@@ -458,13 +442,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
             mma_commit(&bars[bKvFree + 2 * buf + hh]);
           }
-          mma_commit(&bars[bPvLocal]);
           if (g + 1 == seg_end) mma_commit(&bars[bOReady]);
           // The next tile of the same query token: its S right behind this PV.
           if (g + 1 < seg_end) issue_qk(n_tile + 1);
-          // Tell the peer that this CTA's P operand is free again.
-          mbar_wait(&bars[bPvLocal], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-          arrive_peer(peer_pv);
           first = false;
         }
         ++n_seg;
@@ -477,28 +457,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------
-    // Softmax warps: thread i <-> head i <-> TMEM lane i.
+    // Softmax warps: thread i <-> head i <-> TMEM lane i.  This CTA owns the
+    // softmax of token half c of every tile (tokens 64c .. 64c+63); the
+    // partial scores of the other half go to the peer, the peer's partial
+    // for this half comes back, the per-head tile maxima are swapped so both
+    // CTAs keep identical running maxima, and each CTA's P half travels to
+    // the other so both hold all of P for their PV.
     // ------------------------------------------------------------------
     const int i = tid;
-    const bool owner = (i >> 6) == static_cast<int>(c);
-    const int r = i & 63;  // my row in X / alpha / stats (mine as owner, the peer's as shipper)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO, tQ = tmem + lane_base + kColQ;
     const uint32_t peer_x = peer_of(smem_u32(sX), peer);
     const uint32_t peer_p = peer_of(smem_u32(sP), peer);
-    const uint32_t peer_alpha = peer_of(smem_u32(sAlphaIn), peer);
-    const uint32_t peer_stats = peer_of(smem_u32(sStats + r), peer);
+    const uint32_t peer_max = peer_of(smem_u32(sMaxIn), peer);
+    const uint32_t peer_stats = peer_of(smem_u32(sStats), peer);
     const uint32_t pb_xfull = peer_of(smem_u32(&bars[bXFull]), peer);
-    const uint32_t pb_xfree = peer_of(smem_u32(&bars[bXFree]), peer);
     const uint32_t pb_pin = peer_of(smem_u32(&bars[bPIn]), peer);
+    const uint32_t pb_max = peer_of(smem_u32(&bars[bMaxFull]), peer);
     const uint32_t pb_stats0 = peer_of(smem_u32(&bars[bStatsIn]), peer);
-    const uint32_t named = owner ? 2u : 3u;  // 64-thread barrier of my role
+    const int mine0 = static_cast<int>(c) * 64, other0 = static_cast<int>(peer) * 64;
     uint32_t n_tile = 0, n_seg = 0;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // running max (shared by both CTAs) and this half's row sum
     for (int64_t g = span.g_begin; g < span.g_end;) {
       const int qidx = static_cast<int>(g / p.T);
       const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
       const int64_t seg_begin = g;
+      if (i == 0) mbar_expect_tx(&bars[bStatsIn + (n_seg & 1)], 512);
       {
         // Q row i, my half of the dims, into TMEM as packed bf16 pairs.
         const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qidx) * kHeads + i) * kD +
@@ -522,169 +506,162 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       for (; g < seg_end; ++g, ++n_tile) {
         const bool first = g == seg_begin;
+        if (i == 0) {
+          mbar_expect_tx(&bars[bXFull], kXBytes);
+          mbar_expect_tx(&bars[bPIn], kPInBytes);
+          mbar_expect_tx(&bars[bMaxFull], 512);
+        }
         mbar_wait(&bars[bSFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
         __syncwarp();
         tc_fence_after();
-        if (!owner) {
-          // Shipper: my row of the partial S -> staging (in my P operand,
-          // free until my owners write P) -> one bulk copy to the peer's X.
-          if (r == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
+        // 1. The other half of my row of partial scores, pre-scaled, to the
+        //    staging (my P operand: free, my PV of the previous tile is done).
 #pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            uint32_t v[32];
-            tmem_ld32(tS + j * 32, v);
+        for (int j = 0; j < 2; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tS + other0 + j * 32, v);
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(sP + xoff(r, 8 * j + u)) =
-                  make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(named, 64);
-          if (r == 0) {
-            if (n_tile > 0) mbar_wait_cluster(&bars[bXFree], (n_tile - 1) & 1, abort_flag, p.d_error);
-            bulk_to_peer(peer_x, sP, kXBytes, pb_xfull);
-            bulk_commit_and_wait_read();
-            mbar_arrive(&bars[bOutFree]);
-          }
-          // The peer's owners' P rows for my heads and their alphas.
-          mbar_wait(&bars[bPIn], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-          __syncwarp();
-          const float alpha = sAlphaIn[r];
-          if (!first && alpha != 1.f) {
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
-              uint32_t o[32];
-              tmem_ld32(tO + j * 32, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(tO + j * 32, o);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          mbar_arrive(&bars[bPFull]);
-        } else {
-          // Owner: S = my partial + the peer's, masked; running max; P.
-          if (r == 0) mbar_expect_tx(&bars[bXFull], kXBytes);
-          const uint32_t mp = n_tile & 1;
-          mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          uint32_t mk[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mk[j] = sMask[mp * 4 + j];
-          mbar_arrive(&bars[bMaskFree + mp]);
-          mbar_wait(&bars[bXFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-          __syncwarp();
-          float mt = -INFINITY;
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            uint32_t v[32];
-            tmem_ld32(tS + j * 32, v);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float4 x4 = *reinterpret_cast<const float4*>(sX + xoff(r, 8 * j + u));
-              const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int t = 32 * j + 4 * u + e;
-                const bool ok = (mk[e] >> (t >> 2)) & 1u;  // t & 3 == e
-                const float x = (__uint_as_float(v[4 * u + e]) + xs[e]) * p.scale_log2;
-                mt = ok ? fmaxf(mt, x) : mt;
-              }
-            }
-          }
-          float alpha = 1.f;
-          if (mt > m + kLazy || (m == -INFINITY && mt > -INFINITY)) {
-            alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
-            m = mt;
-          }
-          l *= alpha;
-          if (!first && alpha != 1.f) {
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
-              uint32_t o[32];
-              tmem_ld32(tO + j * 32, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(tO + j * 32, o);
-            }
-            tmem_wait_st();
-          }
-          // My P operand still holds the outgoing S until the shippers'
-          // copy has read it.
-          mbar_wait(&bars[bOutFree], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-          __syncwarp();
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            uint32_t v[32];
-            tmem_ld32(tS + j * 32, v);
-            float pv[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const float4 x4 = *reinterpret_cast<const float4*>(sX + xoff(r, 8 * j + u));
-              const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int t = 32 * j + 4 * u + e;
-                const bool ok = (mk[e] >> (t >> 2)) & 1u;
-                const float x = (__uint_as_float(v[4 * u + e]) + xs[e]) * p.scale_log2;
-                const float pe = (ok && m != -INFINITY) ? ex2_approx(x - m) : 0.f;
-                pv[4 * u + e] = pe;
-                l += pe;
-              }
-            }
-            // 32 tokens = 4 units of 8 in P chunk j/2, units 4(j&1) .. +3.
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t off = (j >> 1) * 16384 + swz<128>(i * 128 + (4 * (j & 1) + u) * 16);
-              *reinterpret_cast<uint4*>(sP + off) =
-                  make_uint4(pack_bf16x2(pv[8 * u + 0], pv[8 * u + 1]), pack_bf16x2(pv[8 * u + 2], pv[8 * u + 3]),
-                             pack_bf16x2(pv[8 * u + 4], pv[8 * u + 5]), pack_bf16x2(pv[8 * u + 6], pv[8 * u + 7]));
-            }
-          }
-          float* alpha_out = sAlphaOut + (n_tile & 1) * 64;
-          alpha_out[r] = alpha;
-          fence_proxy_async_smem();
-          named_bar_sync(named, 64);
-          if (r == 0) {
-            arrive_peer(pb_xfree);  // my X rows are read
-            // The peer's P operand is free once its PV of the previous tile is done.
-            if (n_tile > 0) mbar_wait_cluster(&bars[bPvPeer], (n_tile - 1) & 1, abort_flag, p.d_error);
-            const uint32_t rows = static_cast<uint32_t>(c) * 64 * 128;  // my 64 rows of each P chunk
-            bulk_to_peer(peer_p + rows, sP + rows, 8192, pb_pin);
-            bulk_to_peer(peer_p + 16384 + rows, sP + 16384 + rows, 8192, pb_pin);
-            bulk_to_peer(peer_alpha, alpha_out, 256, pb_pin);
-            bulk_commit_and_wait_read();
-          }
-          tc_fence_before();
-          mbar_arrive(&bars[bPFull]);
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(sP + xoff(i, 8 * j + u)) =
+                make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
+                           __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
+                           __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
+                           __float_as_uint(__uint_as_float(v[4 * u + 3]) * p.scale_log2));
         }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (i == 0) {
+          // The peer's X buffer is free: the peer has received this CTA's P
+          // of the previous tile, sent after every read of X.
+          bulk_to_peer(peer_x, sP, kXBytes, pb_xfull);
+          bulk_commit_and_wait_read();
+          mbar_arrive(&bars[bOutFree]);
+        }
+        // 2. Add the peer's partial for my half; mask; local maximum.
+        const uint32_t mp = n_tile & 1;
+        mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+        // Validity of my tokens mine0 + 4b + e is bit b of mk[e].
+        uint32_t mk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mk[e] = sMask[mp * 4 + e] >> (16 * c);
+        mbar_arrive(&bars[bMaskFree + mp]);
+        mbar_wait(&bars[bXFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        // y = scaled S + X (or -inf where masked), written back over my half of S.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tS + mine0 + j * 32, v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 x4 = *reinterpret_cast<const float4*>(sX + xoff(i, 8 * j + u));
+            const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool ok = (mk[e] >> (8 * j + u)) & 1u;
+              const float y = ok ? fmaf(__uint_as_float(v[4 * u + e]), p.scale_log2, xs[e]) : -INFINITY;
+              mx[e] = fmaxf(mx[e], y);
+              v[4 * u + e] = __float_as_uint(y);
+            }
+          }
+          tmem_st32(tS + mine0 + j * 32, v);
+        }
+        const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        tmem_wait_st();
+        // 3. Swap tile maxima with the peer; both update the running max alike.
+        sMaxOut[i] = mloc;
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (i == 0) {
+          bulk_to_peer(peer_max, sMaxOut, 512, pb_max);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        mbar_wait(&bars[bMaxFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        const float mt = fmaxf(mloc, sMaxIn[i]);
+        float alpha = 1.f;
+        if (mt > m + kLazy || (m == -INFINITY && mt > -INFINITY)) {
+          alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+          m = mt;
+        }
+        l *= alpha;
+        if (!first && alpha != 1.f) {
+          __syncwarp();
+#pragma unroll 1
+          for (int j = 0; j < 8; ++j) {
+            uint32_t o[32];
+            tmem_ld32(tO + j * 32, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(tO + j * 32, o);
+          }
+          tmem_wait_st();
+        }
+        // 4. P for my half into my P chunk, once the staging has been read.
+        mbar_wait(&bars[bOutFree], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        uint8_t* pchunk = sP + c * 16384;
+        const float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tS + mine0 + j * 32, v);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              pv[e] = ex2_approx(__uint_as_float(v[8 * u + e]) - mm);
+              ls[e & 3] += pv[e];
+            }
+            *reinterpret_cast<uint4*>(pchunk + swz<128>(i * 128 + (4 * j + u) * 16)) =
+                make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                           pack_bf16x2(pv[6], pv[7]));
+          }
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (i == 0) {
+          // The peer's P chunk for this CTA is free: the peer sent this tile's
+          // X from its P buffer after its previous PV had completed.
+          bulk_to_peer(peer_p + c * 16384, pchunk, kPInBytes, pb_pin);
+          bulk_commit_and_wait_read();
+        }
+        // 5. The peer's P half has landed in my other P chunk.
+        mbar_wait(&bars[bPIn], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        tc_fence_before();
+        mbar_arrive(&bars[bPFull]);
       }
 
-      // Epilogue of this query token (or split): O row i of my dim half / l.
+      // Epilogue of this query token (or split): add the two halves' row
+      // sums, then O row i of my dim half / l.
       const uint32_t sp = n_seg & 1;
-      float linv;
+      sStatsOut[i] = l;
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (i == 0) {
+        bulk_to_peer(peer_stats + sp * 512, sStatsOut, 512, pb_stats0 + sp * 8);
+        bulk_commit_and_wait_read();
+      }
+      mbar_wait(&bars[bStatsIn + sp], (n_seg >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+      const float lt = l + sStats[sp * 128 + i];
+      const float linv = lt > 0.f ? 1.f / lt : 0.f;
       const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
       const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
       const int64_t split = static_cast<int64_t>(p.num_splits[qidx]) + local;
       const bool direct = nsplit == 1;
       const bool split_ok = direct || (split >= 0 && split < p.ws_splits_cap && local < nsplit);
-      if (owner) {
-        linv = l > 0.f ? 1.f / l : 0.f;
-        st_peer_f32(peer_stats + sp * 256, linv);
-        arrive_peer(pb_stats0 + sp * 8);
-        const float lse = l > 0.f ? (m + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
+      if (c == 0) {
+        const float lse = lt > 0.f ? (m + lg2_approx(lt)) * 0.6931471805599453f : -INFINITY;
         const int64_t hrow = static_cast<int64_t>(qidx) * p.h_q + i;
         if (direct)
           p.lse[hrow] = lse;
         else if (split_ok)
           p.ws_lse[split * p.h_q + i] = lse;
         if (!split_ok && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_METADATA);
-        m = -INFINITY;
-        l = 0.f;
-      } else {
-        mbar_wait_cluster(&bars[bStatsIn + sp], (n_seg >> 1) & 1, abort_flag, p.d_error);
-        linv = sStats[sp * 64 + r];
       }
+      m = -INFINITY;
+      l = 0.f;
       mbar_wait(&bars[bOReady], n_seg & 1, abort_flag, p.d_error, kWaitNs);
       __syncwarp();
       tc_fence_after();
@@ -757,24 +734,19 @@ cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap kv_map, scl_map;
+  CUtensorMap kv_map;
   {
-    // The FP8 pool as [tokens][528 bytes]; rows gathered 64 bytes (one 64-dim chunk) or 16 bytes (scales) at a time.
+    // The FP8 pool as [tokens][528 bytes]; rows gathered 256 bytes (one CTA's half of a record's dims) at a time.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRecFp8), static_cast<cuuint64_t>(p.pool_tokens)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRecFp8)};
     const cuuint32_t estr[2] = {1, 1};
-    const cuuint32_t box_d[2] = {64, 1};
-    const cuuint32_t box_s[2] = {16, 1};
-    if (enc(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.kv), dims, strides, box_d, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-    if (enc(&scl_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.kv), dims, strides, box_s, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+    const cuuint32_t box[2] = {256, 1};
+    if (enc(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.kv), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  sparse_decode_pair_kernel<<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map, scl_map);
+  sparse_decode_pair_kernel<<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map);
   return cudaGetLastError();
 }
 
