@@ -47,6 +47,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLazy = 8.0f;
 constexpr uint32_t kXBytes = 128 * 256;         // 128 heads x 64 tokens of fp32 scores (the other CTA's half)
 constexpr uint32_t kPInBytes = 16384;           // the peer's P chunk: 128 heads x 64 tokens bf16
+constexpr uint32_t kXWarpBytes = kXBytes / 4;   // one softmax warp's 32 rows of X
 
 struct PairSmem {
   static constexpr int kKV = 0;                  // 2 buffers x 4 chunks x [128 tokens x 128 B], SW128
@@ -68,9 +69,9 @@ struct PairSmem {
 
 enum PairBar {
   bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
-  bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27, bXFull = 28,
-  bOutFree = 30, bPIn = 31, bPFull = 32, bOReady = 35, bStatsIn = 36 /* [2] */,
-  bMaxFull = 38, bDrain = 39
+  bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27,
+  bPIn = 31, bPMine = 33, bOReady = 35, bStatsIn = 36 /* [2] */, bDrain = 39, bXFull = 40 /* [4 warps] */,
+  bMaxFull = 44 /* [4 warps] */
 };
 
 // TMEM columns: S [0, 128), O [128, 384), Q (bf16 pairs) [384, 512).
@@ -97,6 +98,8 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_peer, const void* src,
                "r"(smem_u32(src)), "r"(bytes), "r"(bar_peer)
                : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
@@ -226,13 +229,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
     mbar_init(&bars[bQFull], 128);
     mbar_init(&bars[bSFull], 1);
-    mbar_init(&bars[bXFull], 1);
-    mbar_init(&bars[bOutFree], 1);
     mbar_init(&bars[bPIn], 1);
-    mbar_init(&bars[bPFull], 128);
+    mbar_init(&bars[bPMine], 128);
     mbar_init(&bars[bOReady], 1);
-    mbar_init(&bars[bMaxFull], 1);
     mbar_init(&bars[bDrain], 1);
+    for (int w = 0; w < 4; ++w) {
+      mbar_init(&bars[bXFull + w], 1);
+      mbar_init(&bars[bMaxFull + w], 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -390,14 +394,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
   } else if (warp == kIssueWarp) {
     // ------------------------------------------------------------------
-    // Tensor-core issue (one thread): S = Q K^T (A = Q in TMEM), then per
-    // tile O += P V followed at once by the next tile's S.
+    // Tensor-core issue (one thread).  Per tile: S = Q K^T (A = Q in TMEM);
+    // O += P V over this CTA's tokens as soon as its P is written, and over
+    // the peer's tokens once the peer's P has landed; the next tile's S
+    // follows at once.
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
       const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
       const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
+      const int mine0 = static_cast<int>(c) * 64, other0 = static_cast<int>(peer) * 64;
       uint32_t n_tile = 0, n_seg = 0;
       bool issued = false;
       auto issue_qk = [&](uint32_t nt) {
@@ -415,6 +422,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
         mma_commit(&bars[bSFull]);
       };
+      auto issue_pv = [&](uint32_t buf, int t0, bool init, bool release) {
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ks = t0 / 16 + q;
+            const uint64_t a = make_smem_desc(p_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128);
+            const uint64_t b =
+                make_smem_desc(kv_base + buf * 65536 + 2 * hh * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
+            mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(init && q == 0));
+          }
+          if (release) mma_commit(&bars[bKvFree + 2 * buf + hh]);
+        }
+      };
       for (int64_t g = span.g_begin; g < span.g_end;) {
         const int qidx = static_cast<int>(g / p.T);
         const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
@@ -428,20 +449,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             issue_qk(n_tile);
             issued = true;
           }
-          mbar_wait(&bars[bPFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-          tc_fence_after();
           const uint32_t buf = n_tile & 1;
-#pragma unroll 1
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t a = make_smem_desc(p_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128);
-              const uint64_t b =
-                  make_smem_desc(kv_base + buf * 65536 + 2 * hh * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
-              mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(first && ks == 0));
-            }
-            mma_commit(&bars[bKvFree + 2 * buf + hh]);
-          }
+          mbar_wait(&bars[bPMine], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          tc_fence_after();
+          issue_pv(buf, mine0, first, false);
+          mbar_wait(&bars[bPIn], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          tc_fence_after();
+          issue_pv(buf, other0, false, true);
           if (g + 1 == seg_end) mma_commit(&bars[bOReady]);
           // The next tile of the same query token: its S right behind this PV.
           if (g + 1 < seg_end) issue_qk(n_tile + 1);
@@ -471,9 +485,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t peer_p = peer_of(smem_u32(sP), peer);
     const uint32_t peer_max = peer_of(smem_u32(sMaxIn), peer);
     const uint32_t peer_stats = peer_of(smem_u32(sStats), peer);
-    const uint32_t pb_xfull = peer_of(smem_u32(&bars[bXFull]), peer);
+    const uint32_t pb_xfull = peer_of(smem_u32(&bars[bXFull + warp]), peer);
     const uint32_t pb_pin = peer_of(smem_u32(&bars[bPIn]), peer);
-    const uint32_t pb_max = peer_of(smem_u32(&bars[bMaxFull]), peer);
+    const uint32_t pb_max = peer_of(smem_u32(&bars[bMaxFull + warp]), peer);
     const uint32_t pb_stats0 = peer_of(smem_u32(&bars[bStatsIn]), peer);
     const int mine0 = static_cast<int>(c) * 64, other0 = static_cast<int>(peer) * 64;
     uint32_t n_tile = 0, n_seg = 0;
@@ -506,38 +520,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       for (; g < seg_end; ++g, ++n_tile) {
         const bool first = g == seg_begin;
-        if (i == 0) {
-          mbar_expect_tx(&bars[bXFull], kXBytes);
-          mbar_expect_tx(&bars[bPIn], kPInBytes);
-          mbar_expect_tx(&bars[bMaxFull], 512);
+        if (lane == 0) {
+          mbar_expect_tx(&bars[bXFull + warp], kXWarpBytes);
+          mbar_expect_tx(&bars[bMaxFull + warp], 128);
         }
         mbar_wait(&bars[bSFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        // The previous tile's P from the peer has landed (this S follows the
+        // PV that waited for it), so the P barrier is in its next phase.
+        if (i == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
+        // This warp's copies of the previous tile out of its rows are read.
+        if (lane == 0) bulk_wait_read();
         __syncwarp();
         tc_fence_after();
-        // 1. The other half of my row of partial scores, pre-scaled, to the
-        //    staging (my P operand: free, my PV of the previous tile is done).
+        // 1. The other half of my row of partial scores, pre-scaled, to this
+        //    warp's staging rows and on to the peer's X.  Warp w stages its 32
+        //    rows as two 4 KB pieces that occupy exactly its rows of the two
+        //    P chunks (free: this CTA's PV of the previous tile is done), so
+        //    every buffer a warp touches in steps 1-4 is its own.
+        uint8_t* stg = sP + (lane >> 4) * 16384 + warp * 4096;
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
           uint32_t v[32];
           tmem_ld32(tS + other0 + j * 32, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(sP + xoff(i, 8 * j + u)) =
+            *reinterpret_cast<uint4*>(stg + xoff(lane & 15, 8 * j + u)) =
                 make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
                            __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
                            __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
                            __float_as_uint(__uint_as_float(v[4 * u + 3]) * p.scale_log2));
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (i == 0) {
-          // The peer's X buffer is free: the peer has received this CTA's P
-          // of the previous tile, sent after every read of X.
-          bulk_to_peer(peer_x, sP, kXBytes, pb_xfull);
-          bulk_commit_and_wait_read();
-          mbar_arrive(&bars[bOutFree]);
+        __syncwarp();
+        if (lane == 0) {
+          // The peer's X rows of this warp are free: this CTA has received
+          // the peer's P of the previous tile (this S follows the PV that
+          // waited for it), which the peer's warp sent after reading X.
+          bulk_to_peer(peer_x + warp * 8192, sP + warp * 4096, 4096, pb_xfull);
+          bulk_to_peer(peer_x + warp * 8192 + 4096, sP + 16384 + warp * 4096, 4096, pb_xfull);
+          bulk_commit();
         }
-        // 2. Add the peer's partial for my half; mask; local maximum.
+        // 2. One pass over my token half: y = scaled S + X (-inf where
+        //    masked), kept in TMEM; P against the running maximum of the
+        //    earlier tiles into my P chunk (free once this warp's staging
+        //    copies have been read); its row sum; the tile maximum.
         const uint32_t mp = n_tile & 1;
         mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
         // Validity of my tokens mine0 + 4b + e is bit b of mk[e].
@@ -545,9 +571,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) mk[e] = sMask[mp * 4 + e] >> (16 * c);
         mbar_arrive(&bars[bMaskFree + mp]);
-        mbar_wait(&bars[bXFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        // y = scaled S + X (or -inf where masked), written back over my half of S.
+        mbar_wait(&bars[bXFull + warp], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        uint8_t* pchunk = sP + c * 16384;
+        float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
           uint32_t v[32];
@@ -565,72 +595,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
           }
           tmem_st32(tS + mine0 + j * 32, v);
-        }
-        const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        tmem_wait_st();
-        // 3. Swap tile maxima with the peer; both update the running max alike.
-        sMaxOut[i] = mloc;
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (i == 0) {
-          bulk_to_peer(peer_max, sMaxOut, 512, pb_max);
-          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        }
-        mbar_wait(&bars[bMaxFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        const float mt = fmaxf(mloc, sMaxIn[i]);
-        float alpha = 1.f;
-        if (mt > m + kLazy || (m == -INFINITY && mt > -INFINITY)) {
-          alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
-          m = mt;
-        }
-        l *= alpha;
-        if (!first && alpha != 1.f) {
-          __syncwarp();
-#pragma unroll 1
-          for (int j = 0; j < 8; ++j) {
-            uint32_t o[32];
-            tmem_ld32(tO + j * 32, o);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(tO + j * 32, o);
-          }
-          tmem_wait_st();
-        }
-        // 4. P for my half into my P chunk, once the staging has been read.
-        mbar_wait(&bars[bOutFree], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        uint8_t* pchunk = sP + c * 16384;
-        const float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          uint32_t v[32];
-          tmem_ld32(tS + mine0 + j * 32, v);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int w = 0; w < 4; ++w) {
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              pv[e] = ex2_approx(__uint_as_float(v[8 * u + e]) - mm);
+              pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
               ls[e & 3] += pv[e];
             }
-            *reinterpret_cast<uint4*>(pchunk + swz<128>(i * 128 + (4 * j + u) * 16)) =
+            *reinterpret_cast<uint4*>(pchunk + swz<128>(i * 128 + (4 * j + w) * 16)) =
                 make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                            pack_bf16x2(pv[6], pv[7]));
           }
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        tmem_wait_st();
+        // 3. Swap this warp's tile maxima with the peer's same warp; both
+        //    CTAs take the same decisions for the same heads.
+        sMaxOut[i] = mloc;
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (i == 0) {
-          // The peer's P chunk for this CTA is free: the peer sent this tile's
-          // X from its P buffer after its previous PV had completed.
-          bulk_to_peer(peer_p + c * 16384, pchunk, kPInBytes, pb_pin);
-          bulk_commit_and_wait_read();
+        __syncwarp();
+        if (lane == 0) {
+          bulk_to_peer(peer_max + warp * 128, sMaxOut + warp * 32, 128, pb_max);
+          bulk_commit();
         }
-        // 5. The peer's P half has landed in my other P chunk.
-        mbar_wait(&bars[bPIn], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        mbar_wait(&bars[bMaxFull + warp], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        const float mt = fmaxf(mloc, sMaxIn[i]);
+        const bool need = mt > m + kLazy || (m == -INFINITY && mt > -INFINITY);
+        if (!__any_sync(0xFFFFFFFFu, need)) {
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        } else {
+          // Rare (the first tile, or a head's maximum grew by more than the
+          // lazy threshold): move the running maximum, rescale O and the row
+          // sum, and recompute this warp's P rows from y.
+          float alpha = 1.f;
+          if (need) {
+            alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+            m = mt;
+          }
+          l *= alpha;
+          if (__any_sync(0xFFFFFFFFu, !first && alpha != 1.f)) {
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {
+              uint32_t o[32];
+              tmem_ld32(tO + j * 32, o);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(tO + j * 32, o);
+            }
+            tmem_wait_st();
+          }
+          mm = m == -INFINITY ? 0.f : m;
+          float lr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int j = 0; j < 2; ++j) {
+            uint32_t v[32];
+            tmem_ld32(tS + mine0 + j * 32, v);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              float pv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
+                lr[e & 3] += pv[e];
+              }
+              *reinterpret_cast<uint4*>(pchunk + swz<128>(i * 128 + (4 * j + w) * 16)) =
+                  make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                             pack_bf16x2(pv[6], pv[7]));
+            }
+          }
+          l += (lr[0] + lr[1]) + (lr[2] + lr[3]);
+        }
+        // 4. This warp's P rows to the peer.
+        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bars[bPFull]);
+        mbar_arrive(&bars[bPMine]);  // the tensor core may start on this CTA's tokens
+        __syncwarp();
+        if (lane == 0) {
+          // The peer's rows for this warp's P are free: the peer sent this
+          // tile's X from them after its previous PV had completed.
+          bulk_to_peer(peer_p + c * 16384 + warp * 4096, pchunk + warp * 4096, 4096, pb_pin);
+          bulk_commit();
+        }
       }
 
       // Epilogue of this query token (or split): add the two halves' row
@@ -690,6 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       tc_fence_before();
       ++n_seg;
     }
+    if (lane == 0) bulk_wait_read();  // this warp's last copies out of shared memory
   }
 
   tc_fence_before();

@@ -144,6 +144,33 @@ def test_large_scores_exercise_rescaling():
     compare(out, lse, w, all_queries(w))
 
 
+@pytest.mark.parametrize("h_q", [64, 128])
+def test_growing_scores_move_the_max_every_tile(h_q):
+    """Every query row shares a component along one unit direction u, and the
+    keys of 128-slot tile t carry 8t along u: each tile's scores sit about ten
+    log2 units above the previous tile's, past the lazy-rescale threshold, so
+    the running maximum moves, and O and the row sums are rescaled, on every
+    tile.  Values stay of order one, so the bf16 P keeps the usual error."""
+    rng = np.random.default_rng(21)
+    b, topk, pool = 2, 1024, 4096
+    idx = _random_idx(rng, b, 1, topk, pool)
+    slot_of = {}
+    for bi in range(b):
+        for t in range(topk):
+            slot_of[int(idx[bi, 0, t])] = t
+    pos = np.array(sorted(slot_of), dtype=np.int64)
+    u = rng.standard_normal(512).astype(np.float32)
+    u /= np.linalg.norm(u)
+    lift = np.array([8.0 * (slot_of[int(x)] // 128) for x in pos], dtype=np.float32)
+    data = rng.standard_normal((pos.shape[0], 512), dtype=np.float32) + lift[:, None] * u[None, :]
+    cfg = synth.Config(99, "custom", b, 1, h_q, pool, topk)
+    q = rng.standard_normal((b, 1, h_q, 512), dtype=np.float32) + 20.0 * u
+    w = synth.Workload(cfg=cfg, q_bits=synth.f32_to_bf16_bits(q), idx=idx.astype(np.int32),
+                       pool_tokens=pool * b, ref_pos=pos, ref_rec=synth.encode_fp8_records(data))
+    out, lse, _ = DeviceWorkload(w).run()
+    compare(out, lse, w, all_queries(w))
+
+
 @pytest.mark.parametrize("num_sms", [1, 3, 152, 100000])
 def test_split_counts_do_not_change_results(num_sms):
     """From one part (no split) to one tile per part (every query split into
