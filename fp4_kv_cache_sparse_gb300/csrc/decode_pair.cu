@@ -55,7 +55,8 @@ struct PairSmem {
                                                  // the outgoing staging of the partial scores
   static constexpr int kX = kP + 32768;          // [128 heads][64 tokens] fp32 from the peer, units swizzled
   static constexpr int kStg = kX + 32768;        // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
-  static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [128 tokens x 8 B] e8m0 scales of this CTA's dims
+  static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [4][32] x 8 B e8m0 scales of this CTA's dims
+                                                        // (token 4l + j at [j][l])
   static constexpr int kBar = kScl + 2 * 1024;   // 48 mbarriers
   static constexpr int kMask = kBar + 48 * 8;    // [2][4] u32 validity bits
   static constexpr int kMaxIn = kMask + 32;      // [128] f32 tile maxima from the peer
@@ -298,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       if (n_tile >= 2) mbar_wait(&bars[bSclFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint2*>(sScl + mp * 1024 + (4 * lane + j) * 8) = sc_cur[j];
+        *reinterpret_cast<uint2*>(sScl + mp * 1024 + (32 * j + lane) * 8) = sc_cur[j];
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[bSclFull + mp]);
@@ -351,6 +352,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           if (n_tile >= 2) {
             mbar_wait(&bars[bKvFree + 2 * buf], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
             mbar_wait(&bars[bKvFree + 2 * buf + 1], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
+            // Hold the tile stores until the previous tile's S is done, so
+            // that they fall in the softmax phase rather than competing with
+            // that S product for shared-memory bandwidth.  (The phase is
+            // unambiguous: S of this tile cannot complete before these stores.)
+            mbar_wait(&bars[bSFull], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitNs);
           }
         }
         mbar_wait(&bars[bStgFull + slot], use & 1, abort_flag, p.d_error, kWaitNs);
@@ -365,7 +371,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           const int item = L + 256 * r;
           const int tt = item >> 4, s = item & 15;
           raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
-          sb[r] = scl[(32 * k + tt) * 8 + (s >> 1)];
+          const int T = 32 * k + tt;  // scales of token T = 4l + j sit at [j][l]
+          sb[r] = scl[(32 * (T & 3) + (T >> 2)) * 8 + (s >> 1)];
           big |= sb[r] > 142u;
         }
         const bool any_big = __any_sync(0xFFFFFFFFu, big);
@@ -379,9 +386,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           else
             dequant_fp8_16(raw[r], sb[r], o);
           uint8_t* chunk = tile + (s >> 2) * 16384;
+          // Segments of odd 64-dim chunks store their upper 16-byte unit
+          // first, so that the 8 lanes of each quarter-warp store to 8
+          // distinct bank groups.
+          const bool odd = (s >> 2) & 1;
           const int u = 2 * (s & 3);
-          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + u * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + 1) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+          const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
+          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + odd) * 16)) = odd ? hi : lo;
+          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + !odd) * 16)) = odd ? lo : hi;
         }
         fence_proxy_async_smem();
         __syncwarp();
