@@ -24,8 +24,9 @@
 // record's dim chunk per row) into a 3-slot staging ring, so the dequantizing
 // warps never have global loads in flight when they publish a chunk.
 //
-// Warps: 0-3 softmax (thread i <-> head i <-> TMEM lane i), 4-11 dequant,
-// 12 loader (indices, validity mask, all TMA), 13 tensor-core issuer.
+// Warps: 0-7 softmax (two per TMEM lane quadrant, one per token-column
+// half), 8-11 dequant, 12 loader (indices, validity mask, scales, TMA row
+// gathers), 13 tensor-core issuer.
 #include <cstdint>
 #include <cuda.h>
 
@@ -40,14 +41,15 @@ constexpr int kPThreads = 448;
 constexpr int kHeads = 128;
 constexpr int kHalf = 256;
 constexpr int kStgSlots = 3;
-constexpr int kProdWarps = 8;
+constexpr int kProdWarps = 4;
+constexpr int kSoftThreads = 256;
 constexpr int kLoaderWarp = 12;
 constexpr int kIssueWarp = 13;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLazy = 8.0f;
 constexpr uint32_t kXBytes = 128 * 256;         // 128 heads x 64 tokens of fp32 scores (the other CTA's half)
 constexpr uint32_t kPInBytes = 16384;           // the peer's P chunk: 128 heads x 64 tokens bf16
-constexpr uint32_t kXWarpBytes = kXBytes / 4;   // one softmax warp's 32 rows of X
+constexpr uint32_t kXWarpBytes = kXBytes / 8;   // one softmax warp's 32 heads x 32 tokens of X
 
 struct PairSmem {
   static constexpr int kKV = 0;                  // 2 buffers x 4 chunks x [128 tokens x 128 B], SW128
@@ -57,13 +59,13 @@ struct PairSmem {
   static constexpr int kStg = kX + 32768;        // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
   static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [4][32] x 8 B e8m0 scales of this CTA's dims
                                                         // (token 4l + j at [j][l])
-  static constexpr int kBar = kScl + 2 * 1024;   // 48 mbarriers
-  static constexpr int kMask = kBar + 48 * 8;    // [2][4] u32 validity bits
-  static constexpr int kMaxIn = kMask + 32;      // [128] f32 tile maxima from the peer
-  static constexpr int kMaxOut = kMaxIn + 512;   // [128] f32 tile maxima for the peer
-  static constexpr int kStats = kMaxOut + 512;   // [2][128] f32 row sums from the peer
-  static constexpr int kStatsOut = kStats + 1024;  // [128] f32 row sums for the peer
-  static constexpr int kScalar = kStatsOut + 512;  // tmem slot, abort flag
+  static constexpr int kBar = kScl + 2 * 1024;   // 64 mbarriers
+  static constexpr int kMask = kBar + 64 * 8;    // [2][4] u32 validity bits
+  static constexpr int kMaxIn = kMask + 32;      // [4 quadrants][2 column halves][32] f32 tile maxima from the peer
+  static constexpr int kMaxOut = kMaxIn + 1024;  // the same, this CTA's, for the peer
+  static constexpr int kStats = kMaxOut + 1024;  // [2 parities][2 column halves][128] f32 row sums from the peer
+  static constexpr int kStatsOut = kStats + 2048;  // [2 column halves][128] f32 row sums for the peer
+  static constexpr int kScalar = kStatsOut + 1024;  // tmem slot, abort flag
   static constexpr int kEnd = kScalar + 16;
   static constexpr int kAlloc = kEnd + 1024;
 };
@@ -71,8 +73,8 @@ struct PairSmem {
 enum PairBar {
   bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
   bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27,
-  bPIn = 31, bPMine = 33, bOReady = 35, bStatsIn = 36 /* [2] */, bDrain = 39, bXFull = 40 /* [4 warps] */,
-  bMaxFull = 44 /* [4 warps] */
+  bPIn = 31, bPMine = 33, bOReady = 35, bStatsIn = 36 /* [2] */, bDrain = 39, bXFull = 40 /* [8 warps] */,
+  bMaxFull = 48 /* [4 quadrants] */
 };
 
 // TMEM columns: S [0, 128), O [128, 384), Q (bf16 pairs) [384, 512).
@@ -223,21 +225,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bars[bSclFull + i], 1);
       mbar_init(&bars[bSclFree + i], kProdWarps);
       mbar_init(&bars[bMaskFull + i], 1);
-      mbar_init(&bars[bMaskFree + i], 128);
+      mbar_init(&bars[bMaskFree + i], kSoftThreads);
       mbar_init(&bars[bStatsIn + i], 1);
       for (int k = 0; k < 4; ++k) mbar_init(&bars[bKvFull + 4 * i + k], kProdWarps);
       for (int h = 0; h < 2; ++h) mbar_init(&bars[bKvFree + 2 * i + h], 1);
     }
-    mbar_init(&bars[bQFull], 128);
+    mbar_init(&bars[bQFull], kSoftThreads);
     mbar_init(&bars[bSFull], 1);
     mbar_init(&bars[bPIn], 1);
-    mbar_init(&bars[bPMine], 128);
+    mbar_init(&bars[bPMine], kSoftThreads);
     mbar_init(&bars[bOReady], 1);
     mbar_init(&bars[bDrain], 1);
-    for (int w = 0; w < 4; ++w) {
-      mbar_init(&bars[bXFull + w], 1);
-      mbar_init(&bars[bMaxFull + w], 1);
-    }
+    for (int w = 0; w < 8; ++w) mbar_init(&bars[bXFull + w], 1);
+    for (int w = 0; w < 4; ++w) mbar_init(&bars[bMaxFull + w], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -332,14 +332,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         sc_cur[j] = sc_nxt[j];
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------------
     // Dequantizers: staging slot (32 tokens x this CTA's 256 dims, raw e4m3)
     // + scales -> bf16 tile rows, into the tile buffer of the tile's parity.
-    // Lane L (0..255) handles items L and L + 256 of a slot; item i is token
-    // i >> 4, 16-dim segment i & 15.
+    // Lane L (0..127) handles items L + 128r (r = 0..3) of a slot; item i is
+    // token i >> 4, 16-dim segment i & 15.
     // ------------------------------------------------------------------
-    const int L = tid - 128;
+    const int L = tid - 256;
     uint32_t n_tile = 0, n_chunk = 0;
     for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
       const uint32_t mp = n_tile & 1;
@@ -363,37 +363,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const uint8_t* stg = sStg + slot * 8192;
         const uint8_t* scl = sScl + mp * 1024;
         uint8_t* tile = sKV + buf * 65536;
-        uint4 raw[2];
-        uint32_t sb[2];
-        bool big = false;
+#pragma unroll 1
+        for (int rb = 0; rb < 4; rb += 2) {
+          uint4 raw[2];
+          uint32_t sb[2];
+          bool big = false;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int item = L + 256 * r;
-          const int tt = item >> 4, s = item & 15;
-          raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
-          const int T = 32 * k + tt;  // scales of token T = 4l + j sit at [j][l]
-          sb[r] = scl[(32 * (T & 3) + (T >> 2)) * 8 + (s >> 1)];
-          big |= sb[r] > 142u;
-        }
-        const bool any_big = __any_sync(0xFFFFFFFFu, big);
+          for (int r = 0; r < 2; ++r) {
+            const int item = L + 128 * (rb + r);
+            const int tt = item >> 4, s = item & 15;
+            raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
+            const int T = 32 * k + tt;  // scales of token T = 4l + j sit at [j][l]
+            sb[r] = scl[(32 * (T & 3) + (T >> 2)) * 8 + (s >> 1)];
+            big |= sb[r] > 142u;
+          }
+          const bool any_big = __any_sync(0xFFFFFFFFu, big);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int item = L + 256 * r;
-          const int t = 32 * k + (item >> 4), s = item & 15;
-          uint32_t o[8];
-          if (!any_big)
-            dequant_fp8_16_small_scale(raw[r], sb[r], o);
-          else
-            dequant_fp8_16(raw[r], sb[r], o);
-          uint8_t* chunk = tile + (s >> 2) * 16384;
-          // Segments of odd 64-dim chunks store their upper 16-byte unit
-          // first, so that the 8 lanes of each quarter-warp store to 8
-          // distinct bank groups.
-          const bool odd = (s >> 2) & 1;
-          const int u = 2 * (s & 3);
-          const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
-          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + odd) * 16)) = odd ? hi : lo;
-          *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + !odd) * 16)) = odd ? lo : hi;
+          for (int r = 0; r < 2; ++r) {
+            const int item = L + 128 * (rb + r);
+            const int t = 32 * k + (item >> 4), s = item & 15;
+            uint32_t o[8];
+            if (!any_big)
+              dequant_fp8_16_small_scale(raw[r], sb[r], o);
+            else
+              dequant_fp8_16(raw[r], sb[r], o);
+            uint8_t* chunk = tile + (s >> 2) * 16384;
+            // Segments of odd 64-dim chunks store their upper 16-byte unit
+            // first, so that the 8 lanes of each quarter-warp store to 8
+            // distinct bank groups.
+            const bool odd = (s >> 2) & 1;
+            const int u = 2 * (s & 3);
+            const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + odd) * 16)) = odd ? hi : lo;
+            *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + !odd) * 16)) = odd ? lo : hi;
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -483,38 +486,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------
-    // Softmax warps: thread i <-> head i <-> TMEM lane i.  This CTA owns the
-    // softmax of token half c of every tile (tokens 64c .. 64c+63); the
-    // partial scores of the other half go to the peer, the peer's partial
-    // for this half comes back, the per-head tile maxima are swapped so both
-    // CTAs keep identical running maxima, and each CTA's P half travels to
-    // the other so both hold all of P for their PV.
+    // Softmax warps 0-7.  Warp w serves the 32 heads of TMEM lane quadrant
+    // qd = w & 3 (lane <-> head 32 qd + lane <-> TMEM lane) and token columns
+    // 32 ch .. 32 ch + 31 (ch = w >> 2) of each 64-token half, so two warps
+    // share each head.  This CTA owns the softmax of token half c of every
+    // tile: each warp sends its columns of the other half's partial scores to
+    // the peer's same warp and receives the peer's for its columns of this
+    // half; the per-head tile maxima of both warps of a quadrant are swapped
+    // with the peer so both CTAs keep identical running maxima; each
+    // quadrant's P rows travel to the peer, so both hold all of P for PV.
     // ------------------------------------------------------------------
-    const int i = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int qd = warp & 3, ch = warp >> 2;
+    const int i = 32 * qd + lane;  // head
+    const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
     const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO, tQ = tmem + lane_base + kColQ;
-    const uint32_t peer_x = peer_of(smem_u32(sX), peer);
-    const uint32_t peer_p = peer_of(smem_u32(sP), peer);
-    const uint32_t peer_max = peer_of(smem_u32(sMaxIn), peer);
-    const uint32_t peer_stats = peer_of(smem_u32(sStats), peer);
-    const uint32_t pb_xfull = peer_of(smem_u32(&bars[bXFull + warp]), peer);
-    const uint32_t pb_pin = peer_of(smem_u32(&bars[bPIn]), peer);
-    const uint32_t pb_max = peer_of(smem_u32(&bars[bMaxFull + warp]), peer);
-    const uint32_t pb_stats0 = peer_of(smem_u32(&bars[bStatsIn]), peer);
+    // Staging block of this warp = rows 32 qd .. 32 qd + 31 of P chunk ch;
+    // the quadrant's P rows of this CTA's chunk are the block of warp (qd, c).
+    const uint32_t stg_off = ch * 16384 + qd * 4096;
     const int mine0 = static_cast<int>(c) * 64, other0 = static_cast<int>(peer) * 64;
+    const int pair_bar = 2 + qd;  // named barrier of the two warps of quadrant qd
     uint32_t n_tile = 0, n_seg = 0;
-    float m = -INFINITY, l = 0.f;  // running max (shared by both CTAs) and this half's row sum
+    float m = -INFINITY, l = 0.f;  // running max (shared by both CTAs) and this warp's part of the row sum
     for (int64_t g = span.g_begin; g < span.g_end;) {
       const int qidx = static_cast<int>(g / p.T);
       const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
       const int64_t seg_begin = g;
-      if (i == 0) mbar_expect_tx(&bars[bStatsIn + (n_seg & 1)], 512);
+      if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bStatsIn + (n_seg & 1)], 1024);
       {
-        // Q row i, my half of the dims, into TMEM as packed bf16 pairs.
+        // Q row i, dims [128 ch, 128 ch + 128) of my half, into TMEM as packed
+        // bf16 pairs.
         const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qidx) * kHeads + i) * kD +
-                                                          static_cast<int>(c) * kHalf);
+                                                          static_cast<int>(c) * kHalf + ch * 128);
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
           uint32_t v[32];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -524,39 +528,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             v[4 * u + 2] = w.z;
             v[4 * u + 3] = w.w;
           }
-          tmem_st32(tQ + j * 32, v);
+          tmem_st32(tQ + 64 * ch + 32 * j, v);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars[bQFull]);
       }
       for (; g < seg_end; ++g, ++n_tile) {
-        const bool first = g == seg_begin;
         if (lane == 0) {
           mbar_expect_tx(&bars[bXFull + warp], kXWarpBytes);
-          mbar_expect_tx(&bars[bMaxFull + warp], 128);
+          if (ch == 0) mbar_expect_tx(&bars[bMaxFull + qd], 256);
         }
         mbar_wait(&bars[bSFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
         // The previous tile's P from the peer has landed (this S follows the
         // PV that waited for it), so the P barrier is in its next phase.
-        if (i == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
-        // This warp's copies of the previous tile out of its rows are read.
+        if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
+        // This warp's copies of the previous tile out of its block are read.
         if (lane == 0) bulk_wait_read();
         __syncwarp();
         tc_fence_after();
-        // 1. The other half of my row of partial scores, pre-scaled, to this
-        //    warp's staging rows and on to the peer's X.  Warp w stages its 32
-        //    rows as two 4 KB pieces that occupy exactly its rows of the two
-        //    P chunks (free: this CTA's PV of the previous tile is done), so
-        //    every buffer a warp touches in steps 1-4 is its own.
-        uint8_t* stg = sP + (lane >> 4) * 16384 + warp * 4096;
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
+        // 1. My columns of the other half's partial scores, pre-scaled, to my
+        //    staging block (free: this CTA's PV of the previous tile is done)
+        //    and on to the peer's same warp.
+        {
           uint32_t v[32];
-          tmem_ld32(tS + other0 + j * 32, v);
+          tmem_ld32(tS + other0 + 32 * ch, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(stg + xoff(lane & 15, 8 * j + u)) =
+            *reinterpret_cast<uint4*>(sP + stg_off + lane * 128 + ((u ^ (lane & 7)) << 4)) =
                 make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
                            __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
                            __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
@@ -565,48 +564,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          // The peer's X rows of this warp are free: this CTA has received
+          // The peer's X block of this warp is free: this CTA has received
           // the peer's P of the previous tile (this S follows the PV that
-          // waited for it), which the peer's warp sent after reading X.
-          bulk_to_peer(peer_x + warp * 8192, sP + warp * 4096, 4096, pb_xfull);
-          bulk_to_peer(peer_x + warp * 8192 + 4096, sP + 16384 + warp * 4096, 4096, pb_xfull);
+          // waited for it), which the peer sent after its warps read X.
+          bulk_to_peer(peer_of(smem_u32(sX + warp * 4096), peer), sP + stg_off, kXWarpBytes,
+                       peer_of(smem_u32(&bars[bXFull + warp]), peer));
           bulk_commit();
         }
-        // 2. One pass over my token half: y = scaled S + X (-inf where
-        //    masked), kept in TMEM; P against the running maximum of the
-        //    earlier tiles into my P chunk (free once this warp's staging
-        //    copies have been read); its row sum; the tile maximum.
+        // 2. One pass over my columns of my token half: y = scaled S + X
+        //    (-inf where masked), kept in TMEM; P against the running maximum
+        //    of the earlier tiles into my P units; its row sum; the maximum.
         const uint32_t mp = n_tile & 1;
         mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-        // Validity of my tokens mine0 + 4b + e is bit b of mk[e].
-        uint32_t mk[4];
+        // Validity of my token mine0 + 32 ch + 4u + e is bit 8e + u of mk.
+        uint32_t mk = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) mk[e] = sMask[mp * 4 + e] >> (16 * c);
+        for (int e = 0; e < 4; ++e) mk |= ((sMask[mp * 4 + e] >> (16 * c + 8 * ch)) & 0xFFu) << (8 * e);
         mbar_arrive(&bars[bMaskFree + mp]);
         mbar_wait(&bars[bXFull + warp], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        // My P units sit in the staging block of warp (qd, c): both warps'
+        // staging copies must have been read.
         if (lane == 0) bulk_wait_read();
-        __syncwarp();
-        uint8_t* pchunk = sP + c * 16384;
+        named_bar_sync(pair_bar, 64);
         float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
+        {
           uint32_t v[32];
-          tmem_ld32(tS + mine0 + j * 32, v);
+          tmem_ld32(tS + mine0 + 32 * ch, v);
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float4 x4 = *reinterpret_cast<const float4*>(sX + xoff(i, 8 * j + u));
+            const float4 x4 =
+                *reinterpret_cast<const float4*>(sX + warp * 4096 + lane * 128 + ((u ^ (lane & 7)) << 4));
             const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const bool ok = (mk[e] >> (8 * j + u)) & 1u;
+              const bool ok = (mk >> (8 * e + u)) & 1u;
               const float y = ok ? fmaf(__uint_as_float(v[4 * u + e]), p.scale_log2, xs[e]) : -INFINITY;
               mx[e] = fmaxf(mx[e], y);
               v[4 * u + e] = __float_as_uint(y);
             }
           }
-          tmem_st32(tS + mine0 + j * 32, v);
+          tmem_st32(tS + mine0 + 32 * ch, v);
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             float pv[8];
@@ -615,101 +614,111 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
               pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
               ls[e & 3] += pv[e];
             }
-            *reinterpret_cast<uint4*>(pchunk + swz<128>(i * 128 + (4 * j + w) * 16)) =
+            *reinterpret_cast<uint4*>(sP + c * 16384 + swz<128>(i * 128 + (4 * ch + w) * 16)) =
                 make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                            pack_bf16x2(pv[6], pv[7]));
           }
         }
         const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         tmem_wait_st();
-        // 3. Swap this warp's tile maxima with the peer's same warp; both
-        //    CTAs take the same decisions for the same heads.
-        sMaxOut[i] = mloc;
+        // 3. Swap tile maxima: this warp's 32 with the peer's same warp; the
+        //    quadrant's four per head (two warps, two CTAs) decide alike in
+        //    both CTAs and both warps.
+        sMaxOut[64 * qd + 32 * ch + lane] = mloc;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          bulk_to_peer(peer_max + warp * 128, sMaxOut + warp * 32, 128, pb_max);
+          bulk_to_peer(peer_of(smem_u32(sMaxIn + 64 * qd + 32 * ch), peer), sMaxOut + 64 * qd + 32 * ch, 128,
+                       peer_of(smem_u32(&bars[bMaxFull + qd]), peer));
           bulk_commit();
         }
-        mbar_wait(&bars[bMaxFull + warp], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        const float mt = fmaxf(mloc, sMaxIn[i]);
+        named_bar_sync(pair_bar, 64);  // the partner warp's maxima are in place
+        mbar_wait(&bars[bMaxFull + qd], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+        const float mt = fmaxf(fmaxf(sMaxOut[64 * qd + lane], sMaxOut[64 * qd + 32 + lane]),
+                               fmaxf(sMaxIn[64 * qd + lane], sMaxIn[64 * qd + 32 + lane]));
         const bool need = mt > m + kLazy || (m == -INFINITY && mt > -INFINITY);
+        float alpha = 1.f;
         if (!__any_sync(0xFFFFFFFFu, need)) {
           l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         } else {
           // Rare (the first tile, or a head's maximum grew by more than the
-          // lazy threshold): move the running maximum, rescale O and the row
-          // sum, and recompute this warp's P rows from y.
-          float alpha = 1.f;
+          // lazy threshold): move the running maximum, rescale the row sum
+          // (and below, my O columns), and recompute my P units from y.
           if (need) {
             alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
             m = mt;
           }
           l *= alpha;
-          if (__any_sync(0xFFFFFFFFu, !first && alpha != 1.f)) {
-#pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
-              uint32_t o[32];
-              tmem_ld32(tO + j * 32, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(tO + j * 32, o);
-            }
-            tmem_wait_st();
-          }
           mm = m == -INFINITY ? 0.f : m;
           float lr[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
-            uint32_t v[32];
-            tmem_ld32(tS + mine0 + j * 32, v);
+          uint32_t v[32];
+          tmem_ld32(tS + mine0 + 32 * ch, v);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              float pv[8];
+          for (int w = 0; w < 4; ++w) {
+            float pv[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
-                lr[e & 3] += pv[e];
-              }
-              *reinterpret_cast<uint4*>(pchunk + swz<128>(i * 128 + (4 * j + w) * 16)) =
-                  make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                             pack_bf16x2(pv[6], pv[7]));
+            for (int e = 0; e < 8; ++e) {
+              pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
+              lr[e & 3] += pv[e];
             }
+            *reinterpret_cast<uint4*>(sP + c * 16384 + swz<128>(i * 128 + (4 * ch + w) * 16)) =
+                make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                           pack_bf16x2(pv[6], pv[7]));
           }
           l += (lr[0] + lr[1]) + (lr[2] + lr[3]);
         }
-        // 4. This warp's P rows to the peer.
+        // alpha == 0 only while m was -inf: O then holds zeros (every P so
+        // far was 0) or, on a segment's first tile, values that this tile's
+        // PV overwrites; either way nothing needs scaling.
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.f && alpha != 0.f)) {
+#pragma unroll 1
+          for (int j = 0; j < 8; ++j) {
+            uint32_t o[16];
+            tmem_ld16(tO + 128 * ch + 16 * j, o);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st16(tO + 128 * ch + 16 * j, o);
+          }
+          tmem_wait_st();
+        }
+        // 4. The quadrant's P rows to the peer, from the warp whose staging
+        //    block holds them (so its own wait covers the copy's reads).
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bars[bPMine]);  // the tensor core may start on this CTA's tokens
-        __syncwarp();
-        if (lane == 0) {
-          // The peer's rows for this warp's P are free: the peer sent this
-          // tile's X from them after its previous PV had completed.
-          bulk_to_peer(peer_p + c * 16384 + warp * 4096, pchunk + warp * 4096, 4096, pb_pin);
+        named_bar_sync(pair_bar, 64);
+        if (ch == static_cast<int>(c) && lane == 0) {
+          // The peer's block for these rows is free: the peer's warps sent
+          // this tile's X from it after its previous PV had completed.
+          bulk_to_peer(peer_of(smem_u32(sP + c * 16384 + qd * 4096), peer), sP + c * 16384 + qd * 4096, 4096,
+                       peer_of(smem_u32(&bars[bPIn]), peer));
           bulk_commit();
         }
       }
 
-      // Epilogue of this query token (or split): add the two halves' row
-      // sums, then O row i of my dim half / l.
+      // Epilogue of this query token (or split): the row sum over both
+      // column halves of both CTAs, added in CTA order so both CTAs agree
+      // bit for bit; then my O columns / l.
       const uint32_t sp = n_seg & 1;
-      sStatsOut[i] = l;
+      sStatsOut[128 * ch + i] = l;
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (i == 0) {
-        bulk_to_peer(peer_stats + sp * 512, sStatsOut, 512, pb_stats0 + sp * 8);
+      named_bar_sync(1, kSoftThreads);
+      if (warp == 0 && lane == 0) {
+        bulk_to_peer(peer_of(smem_u32(sStats + sp * 256), peer), sStatsOut, 1024,
+                     peer_of(smem_u32(&bars[bStatsIn + sp]), peer));
         bulk_commit_and_wait_read();
       }
       mbar_wait(&bars[bStatsIn + sp], (n_seg >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-      const float lt = l + sStats[sp * 128 + i];
+      const float l_mine = sStatsOut[i] + sStatsOut[128 + i];
+      const float l_peer = sStats[sp * 256 + i] + sStats[sp * 256 + 128 + i];
+      const float lt = c == 0 ? l_mine + l_peer : l_peer + l_mine;
       const float linv = lt > 0.f ? 1.f / lt : 0.f;
       const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
       const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
       const int64_t split = static_cast<int64_t>(p.num_splits[qidx]) + local;
       const bool direct = nsplit == 1;
       const bool split_ok = direct || (split >= 0 && split < p.ws_splits_cap && local < nsplit);
-      if (c == 0) {
+      if (c == 0 && ch == 0) {
         const float lse = lt > 0.f ? (m + lg2_approx(lt)) * 0.6931471805599453f : -INFINITY;
         const int64_t hrow = static_cast<int64_t>(qidx) * p.h_q + i;
         if (direct)
@@ -725,10 +734,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       tc_fence_after();
       const int64_t row = static_cast<int64_t>(qidx) * p.h_q + i;
 #pragma unroll 1
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         uint32_t o[32];
-        tmem_ld32(tO + j * 32, o);
-        const int d0 = static_cast<int>(c) * kHalf + j * 32;
+        tmem_ld32(tO + 128 * ch + 32 * j, o);
+        const int d0 = static_cast<int>(c) * kHalf + 128 * ch + 32 * j;
         if (direct) {
           uint4* dst = reinterpret_cast<uint4*>(p.out + row * kD + d0);
 #pragma unroll
