@@ -171,11 +171,13 @@ def test_growing_scores_move_the_max_every_tile(h_q):
     compare(out, lse, w, all_queries(w))
 
 
+@pytest.mark.parametrize("cid", [1, 2])
 @pytest.mark.parametrize("num_sms", [1, 3, 152, 100000])
-def test_split_counts_do_not_change_results(num_sms):
+def test_split_counts_do_not_change_results(num_sms, cid):
     """From one part (no split) to one tile per part (every query split into
-    all its tiles)."""
-    w = synth.make_workload(1, batch=3, workers=1)
+    all its tiles); 64 heads (merged by the combine kernel) and 128 heads
+    (merged inside the decode kernel by the last split to finish)."""
+    w = synth.make_workload(cid, batch=3, workers=1)
     dw = DeviceWorkload(w)
     out, lse, err = dw.run(num_sms=num_sms)
     assert err == 0
