@@ -184,34 +184,6 @@ def time_decode(dw, dec, steps, warmup, flush, dev_barrier=None):
     return ms, t0, t1
 
 
-def time_merge(dec, steps):
-    """CUDA-event duration of the split merge alone: mla_combine over the
-    split partials the last decode call left in the workspace.  The public
-    call also copies single-split query tokens, which the merge inside
-    mla_sparse_decode skips, so this is an upper bound on that merge."""
-    import fp4_kv_cache_sparse_gb300 as mla
-    if dec.num_parts <= 1:
-        return 0.0
-    p = dec.problem
-    splits = p.batch * p.seq_len_q + dec.num_parts
-    o_bytes = (splits * p.h_q * 512 * 4 + 255) // 256 * 256
-    o_part = dec.workspace[:o_bytes].view(torch.float32)
-    lse_part = dec.workspace[o_bytes:o_bytes + splits * p.h_q * 4].view(torch.float32)
-    out = torch.empty((p.batch, p.seq_len_q, p.h_q, 512), dtype=torch.bfloat16, device=dec.device)
-    lse = torch.empty((p.batch, p.seq_len_q, p.h_q), dtype=torch.float32, device=dec.device)
-    stream = torch.cuda.current_stream()
-    for _ in range(3):
-        mla.combine(p, dec.num_splits, o_part, lse_part, out, lse)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for i in range(steps):
-        starts[i].record(stream)
-        mla.combine(p, dec.num_splits, o_part, lse_part, out, lse)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    return statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) * 1e-3
-
-
 def time_e2e(dw, dec, steps, warmup):
     """Through the public API with HOST buffers: pinned q and indices copied
     in, the decode, the output and LSE copied back, every step."""
@@ -370,12 +342,12 @@ def main():
         t = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
-    # The dominant kernel is the decode; its duration is the call's minus the
-    # split merge's (timed alone, an upper bound), both with CUDA events.
-    merge_s = time_merge(dec, max(20, args.steps // 20))
-    kernel_s = max(step_s - merge_s, 1e-9)
-    bound, frac = roofline_of(flops, kvb, kernel_s, pk)
-    per_rank_achieved = flops / kernel_s / 1e12 if bound == "tensor" else kvb / kernel_s / 1e9
+    # The dominant kernel is the decode.  The split merge is launched inside
+    # the same call and cannot be timed apart with events from outside it, so
+    # the achieved figure uses the whole call: it understates the decode
+    # kernel by the merge's share (profiles/ has that share from ncu).
+    bound, frac = roofline_of(flops, kvb, step_s, pk)
+    per_rank_achieved = flops / step_s / 1e12 if bound == "tensor" else kvb / step_s / 1e9
     traffic = profiled_traffic(w.cfg.name)
 
     per_config = {}
@@ -418,9 +390,8 @@ def main():
                      "peak": pk["bf16_tflops"] if bound == "tensor" else pk["hbm_gbs"],
                      "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
                      "frac": frac, "traffic": traffic, "peak_source": pk["source"] + " (burst)",
-                     "kernel": "decode kernel: CUDA-event time of the mla_sparse_decode call minus that of "
-                               "the split merge timed alone",
-                     "call_us": round(step_s * 1e6, 2), "merge_us": round(merge_s * 1e6, 2)},
+                     "kernel": "decode kernel + split merge: CUDA events around the mla_sparse_decode call "
+                               "(the merge is ~4 % of it by the ncu launch list)"},
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 if dec_parts > 1 else 1) * args.steps,
