@@ -54,6 +54,14 @@ def _load():
     lib.oracle_dequant_fp8.restype = None
     lib.oracle_dequant_fp4.argtypes = [P, ctypes.c_longlong, P]
     lib.oracle_dequant_fp4.restype = None
+    lib.oracle_e4m3fn_rne.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3fn_rne.restype = ctypes.c_uint8
+    lib.oracle_e2m1_rne.argtypes = [ctypes.c_double]
+    lib.oracle_e2m1_rne.restype = ctypes.c_uint8
+    lib.oracle_encode_fp8.argtypes = [P, ctypes.c_longlong, P]
+    lib.oracle_encode_fp8.restype = None
+    lib.oracle_encode_fp4.argtypes = [P, ctypes.c_longlong, P]
+    lib.oracle_encode_fp4.restype = None
     lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
     lib.oracle_bf16_rne.restype = ctypes.c_uint16
     lib.oracle_bf16_rne_array.argtypes = [P, ctypes.c_longlong, P]
@@ -100,6 +108,32 @@ def dequant_fp4(records: np.ndarray) -> np.ndarray:
     r = np.ascontiguousarray(records, dtype=np.uint8).reshape(-1, FP4_RECORD_BYTES)
     out = np.empty((r.shape[0], D), dtype=np.float64)
     _load().oracle_dequant_fp4(_ptr(r), r.shape[0], _ptr(out))
+    return out
+
+
+def e4m3fn_rne(x: float) -> int:
+    """Nearest E4M3FN byte (ties to even, saturating at +-448)."""
+    return int(_load().oracle_e4m3fn_rne(float(x)))
+
+
+def e2m1_rne(x: float) -> int:
+    """Nearest e2m1 nibble (ties to even, saturating at +-6)."""
+    return int(_load().oracle_e2m1_rne(float(x)))
+
+
+def encode_fp8(x: np.ndarray) -> np.ndarray:
+    """float64 [n, 512] latents -> uint8 [n, 528] FP8 records (the writer's quantizer)."""
+    x = np.ascontiguousarray(x, dtype=np.float64).reshape(-1, 512)
+    out = np.empty((x.shape[0], 528), dtype=np.uint8)
+    _load().oracle_encode_fp8(_ptr(x), x.shape[0], _ptr(out))
+    return out
+
+
+def encode_fp4(x: np.ndarray) -> np.ndarray:
+    """float64 [n, 512] latents -> uint8 [n, 288] FP4 records (the writer's quantizer)."""
+    x = np.ascontiguousarray(x, dtype=np.float64).reshape(-1, 512)
+    out = np.empty((x.shape[0], 288), dtype=np.uint8)
+    _load().oracle_encode_fp4(_ptr(x), x.shape[0], _ptr(out))
     return out
 
 

@@ -23,6 +23,8 @@
  *
  * Parity pins: every exported function here is pinned by the CPU test suite
  * (decoders against hand-built bytes and library float8 conversions,
+ * encoders by round trips through the decoders, rounding ties, the scale
+ * rule and the library float8 conversion,
  * attention against brute-force dense attention from a library routine and
  * closed forms, combine against the unsplit result).
  */
@@ -108,6 +110,100 @@ void oracle_dequant_fp8(const uint8_t* recs, long long n, double* out) {
 void oracle_dequant_fp4(const uint8_t* recs, long long n, double* out) {
     for (long long t = 0; t < n; ++t)
         oracle_decode_fp4_record(recs + t * ORACLE_FP4_REC, out + t * ORACLE_D);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Record encoders: the quantizer a KV-cache writer applies to a new latent  */
+/* before it stores the record.  [FMLA-KV] "Arithmetic intensity" fixes the  */
+/* formats and block sizes; how a block scale is chosen is this oracle's     */
+/* reading, stated at each function: FP8 takes the smallest power-of-two     */
+/* scale that brings the block maximum within 448 (the "amax/448" choice),   */
+/* FP4 takes amax/6 rounded to E4M3FN.  Elements round to nearest, ties to   */
+/* the even code, saturating at the largest finite value.                    */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest E4M3FN byte to a finite x, ties to the even code, saturating at
+ * +-448; found by scanning every finite code (the sign is kept, so -0.0 gives
+ * 0x80). */
+uint8_t oracle_e4m3fn_rne(double x) {
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {            /* 0x7F is NaN */
+        double d = fabs(oracle_e4m3fn((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Nearest e2m1 nibble to a finite x, ties to the even code, saturating at
+ * +-6, by the same scan. */
+uint8_t oracle_e2m1_rne(double x) {
+    uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    double a = fabs(x);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7; ++c) {
+        double d = fabs(oracle_e2m1((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* 528-byte record from 512 finite values.  Per block of 32: e is the least
+ * integer with amax * 2^-e <= 448 (0 for an all-zero block), clamped to
+ * [-127, 127]; the scale byte is 127 + e; each value is x * 2^-e rounded to
+ * E4M3FN. */
+void oracle_encode_fp8_record(const double* x, uint8_t* rec) {
+    for (int blk = 0; blk < ORACLE_D / 32; ++blk) {
+        const double* xb = x + 32 * blk;
+        double amax = 0.0;
+        for (int j = 0; j < 32; ++j) amax = fmax(amax, fabs(xb[j]));
+        int e = 0;
+        if (amax > 0.0) {
+            int E;
+            frexp(amax, &E);                       /* amax = f 2^E, f in [0.5, 1) */
+            e = E - 10;                            /* amax 2^-e >= 2^9 > 448 */
+            while (ldexp(amax, -e) > 448.0) ++e;
+        }
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+        rec[ORACLE_D + blk] = (uint8_t)(127 + e);
+        for (int j = 0; j < 32; ++j) rec[32 * blk + j] = oracle_e4m3fn_rne(ldexp(xb[j], -e));
+    }
+}
+
+/* 288-byte record from 512 finite values.  Per block of 16: the scale is
+ * amax / 6 rounded to E4M3FN; each value is x / scale rounded to e2m1 (all
+ * +0 when the scale rounds to zero); value 2k goes to the low nibble of byte
+ * k. */
+void oracle_encode_fp4_record(const double* x, uint8_t* rec) {
+    uint8_t codes[ORACLE_D];
+    for (int blk = 0; blk < ORACLE_D / 16; ++blk) {
+        const double* xb = x + 16 * blk;
+        double amax = 0.0;
+        for (int j = 0; j < 16; ++j) amax = fmax(amax, fabs(xb[j]));
+        uint8_t sc = oracle_e4m3fn_rne(amax / 6.0);
+        double s = oracle_e4m3fn(sc);
+        rec[256 + blk] = sc;
+        for (int j = 0; j < 16; ++j) codes[16 * blk + j] = s == 0.0 ? 0 : oracle_e2m1_rne(xb[j] / s);
+    }
+    for (int k = 0; k < 256; ++k) rec[k] = (uint8_t)(codes[2 * k] | (codes[2 * k + 1] << 4));
+}
+
+void oracle_encode_fp8(const double* x, long long n, uint8_t* recs) {
+    for (long long t = 0; t < n; ++t) oracle_encode_fp8_record(x + t * ORACLE_D, recs + t * ORACLE_FP8_REC);
+}
+
+void oracle_encode_fp4(const double* x, long long n, uint8_t* recs) {
+    for (long long t = 0; t < n; ++t) oracle_encode_fp4_record(x + t * ORACLE_D, recs + t * ORACLE_FP4_REC);
 }
 
 /* ------------------------------------------------------------------------ */

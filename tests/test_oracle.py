@@ -378,3 +378,111 @@ def test_joint_softmax_is_the_merge_of_main_and_extra():
                           np.stack([main["lse"].reshape(4), extra["lse"].reshape(4)]))
     np.testing.assert_allclose(o, joint["out_f64"].reshape(4, D), rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(l, joint["lse"].reshape(4), atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Record encoders (the KV-cache writer's quantizer).
+# --------------------------------------------------------------------------
+
+def _e4m3_values():
+    return np.array([oracle.e4m3fn(c) for c in range(0x7F)])  # finite non-negative codes
+
+
+def test_e4m3fn_rne_round_trips_every_code_and_matches_torch():
+    """Every finite code decodes and re-encodes to itself (both signs); on
+    random in-range values the nearest-even rounding agrees with PyTorch's
+    float64 -> float8_e4m3fn conversion."""
+    for c in list(range(0x7F)) + [0x80 | c for c in range(0x7F)]:
+        assert oracle.e4m3fn_rne(oracle.e4m3fn(c)) == c
+    rng = np.random.default_rng(5)
+    x = rng.uniform(-448, 448, 4000) * 2.0 ** rng.integers(-12, 1, 4000)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3fn_rne(v) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_e4m3fn_rne_ties_go_to_the_even_code_and_saturate():
+    vals = _e4m3_values()
+    for c in range(0x7E):
+        mid = (vals[c] + vals[c + 1]) / 2.0
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3fn_rne(mid) == even
+        assert oracle.e4m3fn_rne(-mid) == 0x80 | even
+    assert oracle.e4m3fn_rne(448.0) == 0x7E
+    assert oracle.e4m3fn_rne(1e30) == 0x7E
+    assert oracle.e4m3fn_rne(-1e30) == 0xFE
+    assert oracle.e4m3fn_rne(-0.0) == 0x80
+
+
+def test_e2m1_rne_codes_ties_and_saturation():
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c, v in enumerate(grid):
+        assert oracle.e2m1_rne(v) == c and oracle.e2m1_rne(-v) == 8 | c
+    for c in range(7):
+        mid = (grid[c] + grid[c + 1]) / 2.0
+        assert oracle.e2m1_rne(mid) == (c if c % 2 == 0 else c + 1)
+    assert oracle.e2m1_rne(7.0) == 7 and oracle.e2m1_rne(100.0) == 7 and oracle.e2m1_rne(-9.0) == 15
+
+
+def _fp8_records_with_full_blocks(rng, n):
+    """Random FP8 records whose every block holds a +-448 code (0x7E/0xFE),
+    so that the block maximum fixes the scale."""
+    rec = rng.integers(0, 256, (n, 528)).astype(np.uint8)
+    data = rec[:, :512]
+    data[(data & 0x7F) == 0x7F] ^= 0x01          # no NaN codes
+    for b in range(16):
+        pos = 32 * b + rng.integers(0, 32, n)
+        data[np.arange(n), pos] = np.where(rng.random(n) < 0.5, 0x7E, 0xFE)
+    rec[:, 512:] = rng.integers(100, 150, (n, 16))
+    return rec
+
+
+def test_encode_fp8_inverts_decode_when_the_maximum_is_448():
+    rng = np.random.default_rng(6)
+    rec = _fp8_records_with_full_blocks(rng, 64)
+    assert np.array_equal(oracle.encode_fp8(oracle.dequant_fp8(rec)), rec)
+
+
+def test_encode_fp8_scale_is_the_least_power_of_two_and_rounding_is_within_half_a_step():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((50, 512)) * 2.0 ** rng.integers(-20, 20, (50, 1))
+    x[3, 32:64] = 0.0                          # an all-zero block
+    rec = oracle.encode_fp8(x)
+    e = rec[:, 512:].astype(np.int64) - 127
+    amax = np.abs(x.reshape(50, 16, 32)).max(axis=2)
+    nz = amax > 0
+    assert np.all(amax[nz] * 2.0 ** -e[nz] <= 448.0)
+    assert np.all(amax[nz] * 2.0 ** -(e[nz] - 1) > 448.0)
+    assert rec[3, 513] == 127                  # zero block: scale 1
+    assert np.all((rec[3, 32:64] & 0x7F) == 0)
+    # |decode(encode(x)) - x| <= half the E4M3 step at the scaled value's binade.
+    y = x * 2.0 ** -np.repeat(e, 32, axis=1)
+    binade = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** -6)))
+    half_step = 2.0 ** (binade - 4) * 2.0 ** np.repeat(e, 32, axis=1)
+    err = np.abs(oracle.dequant_fp8(rec) - x)
+    assert np.all(err <= half_step * (1 + 1e-12))
+
+
+def test_encode_fp4_inverts_decode_when_a_block_holds_6():
+    rng = np.random.default_rng(8)
+    n = 40
+    rec = rng.integers(0, 256, (n, 288)).astype(np.uint8)
+    # Scales: finite, non-zero E4M3 codes whose value times 6 stays exact.
+    rec[:, 256:] = rng.integers(0x20, 0x60, (n, 32))
+    codes = np.stack([rec[:, :256] & 0xF, rec[:, :256] >> 4], axis=2).reshape(n, 512)
+    for b in range(32):
+        pos = 16 * b + rng.integers(0, 16, n)
+        codes[np.arange(n), pos] = np.where(rng.random(n) < 0.5, 0x7, 0xF)
+    codes[codes == 0x8] = 0x0                  # -0 and +0 decode alike; keep +0
+    rec[:, :256] = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(oracle.encode_fp4(oracle.dequant_fp4(rec)), rec)
+
+
+def test_encoders_agree_with_the_test_input_quantizer():
+    """The harness quantizer (numpy, its own code) and the oracle (C, a scan
+    over codes) apply the same rule to bf16-valued inputs."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((30, 512)).astype(np.float32) * 2.0 ** rng.integers(-10, 10, (30, 1)).astype(np.float32)
+    x = oracle.bf16_to_f64(synth.f32_to_bf16_bits(x)).astype(np.float32)
+    assert np.array_equal(oracle.encode_fp8(x), synth.encode_fp8_records(x))
+    assert np.array_equal(oracle.encode_fp4(x), synth.encode_fp4_records(x))
