@@ -184,6 +184,42 @@ def time_decode(dw, dec, steps, warmup, flush, dev_barrier=None):
     return ms, t0, t1
 
 
+def time_kv_writer(dev, pk, steps, warmup, flush, tokens=1 << 20):
+    """The KV-cache writer (mla_kv_write) on `tokens` new tokens scattered to
+    a random permutation of the pool's slots, FP8 and FP4: CUDA-event time
+    per call (inputs of 1 GiB, above L2; L2 flushed between calls), and the
+    HBM roofline of its algorithmic bytes (bf16 latents read, records
+    written)."""
+    import fp4_kv_cache_sparse_gb300 as mla
+    g = torch.Generator(device=dev).manual_seed(1234)
+    lat = (torch.randn((tokens, 512), generator=g, device=dev) * 0.05).to(torch.bfloat16)
+    slots = torch.randperm(tokens, generator=g, device=dev).to(torch.int32)
+    res = {}
+    for name, fmt, rec in (("fp8_528", mla.KV_FP8_528, 528), ("fp4_288", mla.KV_FP4_288, 288)):
+        pool = torch.empty((tokens, rec), dtype=torch.uint8, device=dev)
+        for _ in range(warmup):
+            mla.kv_write(lat, slots, pool, fmt)
+        stream = torch.cuda.current_stream()
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            mla.kv_write(lat, slots, pool, fmt)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        t = statistics.mean(ms) * 1e-3
+        nbytes = tokens * (1024 + rec)
+        res[name] = {"tokens": tokens, "us": round(t * 1e6, 2), "gbs": round(nbytes / t / 1e9, 1),
+                     "roofline_frac": round(nbytes / t / 1e9 / pk["hbm_gbs"], 4), "bytes": nbytes}
+        del pool
+    del lat, slots
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_e2e(dw, dec, steps, warmup):
     """Through the public API with HOST buffers: pinned q and indices copied
     in, the decode, the output and LSE copied back, every step."""
@@ -351,9 +387,11 @@ def main():
     traffic = profiled_traffic(w.cfg.name)
 
     per_config = {}
+    kv_writer = None
     if not args.no_secondary:
         del dw, dec
         torch.cuda.empty_cache()
+        kv_writer = time_kv_writer(dev, pk, max(20, args.steps // 50), args.warmup, flush)
         for cid in SECONDARY:
             wc = synth.make_workload(cid, seed=synth.SEED_BASE + cid + 7919 * rank)
             f2, b2 = synth.flops(wc), synth.kv_bytes(wc)
@@ -398,6 +436,7 @@ def main():
         "clocks": clocks.summary(t0, t1) if clocks else None,
         "cpu_baseline": cpu,
         "per_config": per_config,
+        "kv_writer": kv_writer,
     }
     print(json.dumps(line))
 

@@ -16,7 +16,7 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MLAError", "Problem", "load", "get_metadata", "sparse_decode", "combine", "dequantize",
+    "MLAError", "Problem", "load", "get_metadata", "sparse_decode", "combine", "dequantize", "kv_write",
     "SparseMLADecoder", "decode", "KV_NONE", "KV_FP8_528", "KV_FP4_288", "KV_BF16",
     "DEVERR_BAD_INDEX", "DEVERR_TIMEOUT", "DEVERR_BAD_METADATA", "SCHED_INTS",
 ]
@@ -79,9 +79,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_sparse_decode.argtypes = [PP, P, P, P, P, P, P, P, I32, P, SZ, P, P, P, P]
     lib.mla_combine.argtypes = [PP, P, P, P, P, P, P]
     lib.mla_dequantize.argtypes = [I32, P, I64, P, P]
+    lib.mla_kv_write.argtypes = [I32, P, P, I64, P, I64, P, P]
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
-    for f in (lib.mla_get_metadata, lib.mla_sparse_decode, lib.mla_combine, lib.mla_dequantize):
+    for f in (lib.mla_get_metadata, lib.mla_sparse_decode, lib.mla_combine, lib.mla_dequantize, lib.mla_kv_write):
         f.restype = ctypes.c_int
     if path == _build.LIB:
         _lib = lib
@@ -138,6 +139,20 @@ def combine(problem: Problem, num_splits, o_partial, lse_partial, out, lse, stre
     lib = load()
     _check(lib.mla_combine(ctypes.byref(problem), _ptr(num_splits), _ptr(o_partial), _ptr(lse_partial),
                            _ptr(out), _ptr(lse), _stream(stream)), "mla_combine")
+
+
+def kv_write(latents: torch.Tensor, slots: torch.Tensor, pool: torch.Tensor, kv_format: int = KV_FP8_528,
+             num_pages: int = None, error: torch.Tensor = None, stream=None) -> None:
+    """Quantize bf16 latents [n, 512] into FP8 (528-byte) or FP4 (288-byte)
+    records and store each at its slot (page*64 + offset, -1 = skip) of the
+    uint8 pool [num_pages, 64, record] (or [tokens, record])."""
+    lib = load()
+    rec = FP8_RECORD_BYTES if kv_format == KV_FP8_528 else FP4_RECORD_BYTES
+    if num_pages is None:
+        num_pages = pool.numel() // (PAGE_SIZE * rec)
+    n = latents.shape[0] if latents.dim() > 0 else 0
+    _check(lib.mla_kv_write(kv_format, _ptr(latents), _ptr(slots), n, _ptr(pool), num_pages, _ptr(error),
+                            _stream(stream)), "mla_kv_write")
 
 
 def dequantize(records: torch.Tensor, kv_format: int = KV_FP8_528, stream=None) -> torch.Tensor:

@@ -19,7 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmla.so")
-SOURCES = ["api.cu", "metadata.cu", "decode.cu", "decode_pair.cu", "combine.cu", "dequant.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "metadata.cu", "decode.cu", "decode_pair.cu", "combine.cu", "dequant.cu", "noalloc.cu", "kv_write.cu"]
 HEADERS = ["mla_device.cuh", "mla_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -239,4 +239,23 @@ mla_status_t mla_dequantize(int32_t kv_format, const void* records, int64_t n, v
   return MLA_OK;
 }
 
+mla_status_t mla_kv_write(int32_t kv_format, const void* latents, const int32_t* slots, int64_t n, void* pool,
+                          int64_t num_pages, int32_t* d_error, mla_stream_t stream) {
+  if (kv_format != MLA_KV_FP8_528 && kv_format != MLA_KV_FP4_288) {
+    return kv_format == MLA_KV_BF16 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+  }
+  if (n < 0 || num_pages < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (latents == nullptr || slots == nullptr || pool == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(latents) || !aligned16(pool) || (reinterpret_cast<uintptr_t>(slots) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (n * MLA_HEAD_DIM >= (int64_t(1) << 40)) return MLA_ERR_UNSUPPORTED;
+  const int64_t cap = int64_t(1) << 31;
+  const int64_t pool_tokens = num_pages * MLA_PAGE_SIZE < cap ? num_pages * MLA_PAGE_SIZE : cap;
+  if (launch_kv_write(kv_format, static_cast<const uint16_t*>(latents), slots, n, static_cast<uint8_t*>(pool),
+                      pool_tokens, d_error, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 }  // extern "C"

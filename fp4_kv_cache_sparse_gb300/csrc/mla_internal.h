@@ -55,4 +55,7 @@ cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, con
 
 cudaError_t launch_dequant(int kv_format, const uint8_t* records, int64_t n, uint16_t* out, cudaStream_t stream);
 
+cudaError_t launch_kv_write(int kv_format, const uint16_t* latents, const int32_t* slots, int64_t n, uint8_t* pool,
+                            int64_t pool_tokens, int32_t* d_error, cudaStream_t stream);
+
 }  // namespace mla

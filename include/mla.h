@@ -210,6 +210,29 @@ mla_status_t mla_sparse_decode_noalloc(const mla_problem_t* problem,
                                        void* out, float* lse, int32_t* d_error,
                                        mla_stream_t stream);
 
+/*
+ * KV-cache writer: quantize new tokens' latents into records and store each
+ * at its slot of the paged pool -- the step that fills the cache the decode
+ * reads ("Arithmetic intensity": 528-byte FP8 records, e4m3 data plus one
+ * e8m0 scale per 32 values; 288-byte FP4 records, e2m1 data with the even
+ * index in the low nibble plus one e4m3 scale per 16 values).  Block scales:
+ * FP8 uses 2^e for the least e with amax * 2^-e <= 448 (scale byte 127 + e;
+ * 127 for an all-zero block; e clamped to [-127, 127]); FP4 uses amax / 6
+ * rounded to E4M3FN (a zero scale stores all-zero data).  Every element rounds
+ * to nearest, ties to even, saturating at the format's largest finite value.
+ *   kv_format  MLA_KV_FP8_528 or MLA_KV_FP4_288.
+ *   latents    bf16 [n][512] (device, 16-byte aligned), finite values.
+ *   slots      int32 [n] (device): page * 64 + offset; -1 = skip.  Slots
+ *              < -1 or >= num_pages * 64 are skipped and flagged
+ *              (MLA_DEVERR_BAD_INDEX).
+ *   pool       uint8 [num_pages][64][528 or 288] (device, 16-byte aligned);
+ *              only the addressed records are written.  Two tokens with the
+ *              same slot race.
+ *   d_error    device int32 or NULL, as in mla_sparse_decode.
+ */
+mla_status_t mla_kv_write(int32_t kv_format, const void* latents, const int32_t* slots, int64_t n, void* pool,
+                          int64_t num_pages, int32_t* d_error, mla_stream_t stream);
+
 /* Static description of a status code. */
 const char* mla_status_string(mla_status_t status);
 

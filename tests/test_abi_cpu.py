@@ -154,6 +154,22 @@ def test_combine_and_dequantize_argument_checks(lib):
     assert lib.mla_dequantize(mla.KV_FP8_528, A, -1, A, None) == INVALID
 
 
+def test_kv_write_argument_checks(lib):
+    """Validation before any launch (no GPU needed): formats, sizes,
+    pointers, alignment; n = 0 is a no-op."""
+    A = ctypes.c_void_p(1 << 20)
+    I = ctypes.c_void_p((1 << 20) + 64)
+    assert lib.mla_kv_write(mla.KV_BF16, A, I, 4, A, 8, None, None) == UNSUPPORTED
+    assert lib.mla_kv_write(0, A, I, 4, A, 8, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP8_528, A, I, -1, A, 8, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP8_528, A, I, 4, A, -1, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP8_528, None, I, 4, A, 8, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP4_288, A, None, 4, A, 8, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP8_528, ctypes.c_void_p((1 << 20) + 8), I, 4, A, 8, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP8_528, A, ctypes.c_void_p((1 << 20) + 2), 4, A, 8, None, None) == INVALID
+    assert lib.mla_kv_write(mla.KV_FP8_528, A, I, 0, A, 8, None, None) == 0
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
