@@ -74,6 +74,9 @@ CONFIGS = [
     Config(3, "fp8_fp4_b64_h64", 64, 1, 64, 65536, 2048, extra_pool=16384, extra_topk=512),
     Config(4, "long_dense_b32_h16", 32, 1, 16, 1048576, 65536, contiguous=True),
     Config(5, "long_sparse_b32_h16", 32, 1, 16, 1048576, 8192),
+    # Prefill-shaped: one sequence, 1024 query tokens each with its own 2048
+    # indices (the same index semantics at seq_len_q >> 1).
+    Config(6, "prefill_b1_s1024_h128", 1, 1024, 128, 65536, 2048, neg=20, recent_window=4096),
 ]
 BY_NAME = {c.name: c for c in CONFIGS}
 

@@ -32,7 +32,7 @@ def test_reduced_configs_all_queries(cid):
     compare(out, lse, w, all_queries(w))
 
 
-@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5, 6])
 def test_full_size_sampled_queries(cid):
     """The full workload in the launch configuration the benchmark times;
     sampled query tokens against the oracle, the rest checked for finiteness

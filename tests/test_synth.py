@@ -7,7 +7,7 @@ import oracle
 import synth
 
 
-@pytest.mark.parametrize("cid", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cid", [0, 1, 2, 3, 4, 5, 6])
 def test_index_structure(cid):
     cfg = synth.CONFIGS[cid]
     w = synth.make_workload(cid, batch=min(cfg.batch, 2), workers=1)
