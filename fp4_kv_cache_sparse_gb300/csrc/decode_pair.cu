@@ -5,28 +5,27 @@
 // What it computes is the same as decode.cu ("flops/flashmla-decode-fp8-fp4-kv",
 // "Arithmetic intensity" and "Workarounds"; "deepseek-ai/FlashMLA", "How to use
 // it"), for an FP8 main cache without an extra cache.  The layout differs:
-// heads are the MMA's M dimension (all 128 of them), so both products run on
-// the tensor core with N = 128 per instruction instead of the 64-head,
-// tokens-on-M form whose small N leaves the tensor core waiting on shared
-// memory.  O for 128 heads x 512 dims would fill all of TMEM, so CTA c of the
-// pair owns dims [256c, 256c + 256): its half of every record, of Q (kept in
-// TMEM as the A operand of S = Q K^T), of the bf16 tile and of O.  Each CTA's
-// S is a partial sum over its dims; CTA c computes the softmax of token half
-// c of every tile for all heads: it sends the peer its partial scores of the
-// other token half and receives the peer's for its own half (bulk
-// asynchronous copies between the two shared memories, completing on the
-// receiver's mbarrier), the two CTAs swap per-head tile maxima so that they
-// keep identical running maxima (and rescale factors), and each sends the
-// other its half of P, so both hold all of P for their PV.  Q in TMEM leaves
-// shared memory for a double-buffered bf16 tile: the dequantizers fill the
-// next tile while the current one is in use.  Records reach shared memory by
-// TMA row gathers (tile::gather4, 4 tokens per instruction, 64 bytes of one
-// record's dim chunk per row) into a 3-slot staging ring, so the dequantizing
-// warps never have global loads in flight when they publish a chunk.
+// heads are the MMA's M dimension (all 128 of them).  O for 128 heads x 512
+// dims would fill all of TMEM, so CTA c of the pair owns dims [256c, 256c+256):
+// its half of every record, of Q, of the bf16 tile and of O.  Each CTA's S is
+// a partial sum over its dims.  A scheduled 128-token tile is processed as two
+// 64-token sub-tiles, so that S fits TMEM twice: the tensor core computes the
+// next sub-tile's S = Q K^T (Q in shared memory) while the softmax warps work
+// on the current one.  CTA c computes the softmax of token quarter c of every
+// sub-tile (tokens 32c .. 32c+31) for all heads: it sends the peer its
+// partial scores of the peer's quarter and receives the peer's for its own
+// (bulk asynchronous copies between the two shared memories, completing on
+// the receiver's mbarrier), the two CTAs swap per-head tile maxima so that
+// they keep identical running maxima (and rescale factors), and each sends
+// the other its part of P, so both hold all of P for their O += P V.  The
+// bf16 tile is triple-buffered; records reach shared memory by TMA row
+// gathers (tile::gather4, 4 tokens per instruction, 256 bytes of a record per
+// row) into a 3-slot staging ring, so the dequantizing warps never have
+// global loads in flight when they publish a slot.
 //
-// Warps: 0-7 softmax (two per TMEM lane quadrant, one per token-column
-// half), 8-11 dequant, 12 loader (indices, validity mask, scales, TMA row
-// gathers), 13 tensor-core issuer.
+// Warps: 0-7 softmax (two per TMEM lane quadrant, one per 16-token column
+// half of the quarter), 8-11 dequant, 12 loader (indices, validity mask,
+// scales, TMA row gathers), 13 tensor-core issuer.
 #include <cstdint>
 #include <cuda.h>
 
@@ -41,24 +40,26 @@ constexpr int kPThreads = 448;
 constexpr int kHeads = 128;
 constexpr int kHalf = 256;
 constexpr int kStgSlots = 3;
+constexpr int kKvBufs = 3;
 constexpr int kProdWarps = 4;
 constexpr int kSoftThreads = 256;
 constexpr int kLoaderWarp = 12;
 constexpr int kIssueWarp = 13;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLazy = 8.0f;
-constexpr uint32_t kXBytes = 128 * 256;         // 128 heads x 64 tokens of fp32 scores (the other CTA's half)
-constexpr uint32_t kPInBytes = 16384;           // the peer's P chunk: 128 heads x 64 tokens bf16
-constexpr uint32_t kXWarpBytes = kXBytes / 8;   // one softmax warp's 32 heads x 32 tokens of X
+constexpr uint32_t kXWarpBytes = 32 * 64;       // one softmax warp's 32 heads x 16 tokens of fp32 scores
+constexpr uint32_t kPQuadBytes = 32 * 64;       // a quadrant's 32 heads x 32 tokens of bf16 P
+constexpr uint32_t kPInBytes = 4 * kPQuadBytes;  // the peer's quarter of P
 
 struct PairSmem {
-  static constexpr int kKV = 0;                  // 2 buffers x 4 chunks x [128 tokens x 128 B], SW128
-  static constexpr int kP = kKV + 2 * 65536;     // 2 chunks x [128 heads x 128 B] (64 tokens each); also
-                                                 // the outgoing staging of the partial scores
-  static constexpr int kX = kP + 32768;          // [128 heads][64 tokens] fp32 from the peer, units swizzled
-  static constexpr int kStg = kX + 32768;        // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
+  static constexpr int kQ = 0;                   // Q: 4 chunks x [128 heads x 128 B] bf16 (this CTA's dims), SW128
+  static constexpr int kKV = kQ + 65536;         // 3 buffers x 4 chunks x [64 tokens x 128 B], SW128
+  static constexpr int kP = kKV + kKvBufs * 32768;  // 2 chunks (32 tokens each) x [128 heads x 64 B] bf16, SW64;
+                                                 // also the outgoing staging of the partial scores
+  static constexpr int kX = kP + 16384;          // 8 warps x [32 heads x 16 tokens] fp32 from the peer, SW64 units
+  static constexpr int kStg = kX + 16384;        // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
   static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [4][32] x 8 B e8m0 scales of this CTA's dims
-                                                        // (token 4l + j at [j][l])
+                                                        // (token 4l + j of a 128-token tile at [j][l])
   static constexpr int kBar = kScl + 2 * 1024;   // 64 mbarriers
   static constexpr int kMask = kBar + 64 * 8;    // [2][4] u32 validity bits
   static constexpr int kMaxIn = kMask + 32;      // [4 quadrants][2 column halves][32] f32 tile maxima from the peer
@@ -72,13 +73,13 @@ struct PairSmem {
 
 enum PairBar {
   bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
-  bKvFull = 14 /* [2][4] */, bKvFree = 22 /* [2][2] */, bQFull = 26, bSFull = 27,
-  bPIn = 31, bPMine = 33, bOReady = 35, bStatsIn = 36 /* [2] */, bDrain = 39, bXFull = 40 /* [8 warps] */,
-  bMaxFull = 48 /* [4 quadrants] */
+  bKvFull = 14 /* [3 buffers] */, bKvFree = 17 /* [3] */, bQFull = 20, bSFull = 21 /* [2 S buffers] */,
+  bSUsed = 23 /* [2] */, bPMine = 25, bPIn = 26, bPvDone = 27, bOReady = 28, bStatsIn = 29 /* [2] */, bDrain = 31,
+  bXFull = 32 /* [8 warps] */, bMaxFull = 40 /* [4 quadrants] */
 };
 
-// TMEM columns: S [0, 128), O [128, 384), Q (bf16 pairs) [384, 512).
-constexpr uint32_t kColS = 0, kColO = 128, kColQ = 384;
+// TMEM columns: S [0, 128) as two 64-column buffers, O [128, 384).
+constexpr uint32_t kColS = 0, kColO = 128;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -124,18 +125,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M rows (lanes) x K
-// columns of packed bf16 pairs.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -167,11 +156,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// Byte offset of 16-byte unit u (0..15) of row r in a [rows][256 B] block
-// whose units are XOR-swizzled by the row, so that consecutive rows read at
-// the same logical unit spread over the bank groups.
-__device__ __forceinline__ uint32_t xoff(int r, int u) { return r * 256 + ((u ^ (r & 15)) << 4); }
-
 struct PSpan {
   int64_t g_begin, g_end;
   int first_local_split;
@@ -195,6 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   using L = PairSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + L::kQ;
   uint8_t* sKV = smem + L::kKV;
   uint8_t* sP = smem + L::kP;
   uint8_t* sX = smem + L::kX;
@@ -227,13 +212,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bars[bMaskFull + i], 1);
       mbar_init(&bars[bMaskFree + i], kSoftThreads);
       mbar_init(&bars[bStatsIn + i], 1);
-      for (int k = 0; k < 4; ++k) mbar_init(&bars[bKvFull + 4 * i + k], kProdWarps);
-      for (int h = 0; h < 2; ++h) mbar_init(&bars[bKvFree + 2 * i + h], 1);
+      mbar_init(&bars[bSFull + i], 1);
+      mbar_init(&bars[bSUsed + i], kSoftThreads);
+    }
+    for (int b = 0; b < kKvBufs; ++b) {
+      mbar_init(&bars[bKvFull + b], 2 * kProdWarps);  // two 32-token slots per 64-token sub-tile
+      mbar_init(&bars[bKvFree + b], 1);
     }
     mbar_init(&bars[bQFull], kSoftThreads);
-    mbar_init(&bars[bSFull], 1);
-    mbar_init(&bars[bPIn], 1);
     mbar_init(&bars[bPMine], kSoftThreads);
+    mbar_init(&bars[bPIn], 1);
+    mbar_init(&bars[bPvDone], 1);
     mbar_init(&bars[bOReady], 1);
     mbar_init(&bars[bDrain], 1);
     for (int w = 0; w < 8; ++w) mbar_init(&bars[bXFull + w], 1);
@@ -335,147 +324,146 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------------
     // Dequantizers: staging slot (32 tokens x this CTA's 256 dims, raw e4m3)
-    // + scales -> bf16 tile rows, into the tile buffer of the tile's parity.
-    // Lane L (0..127) handles items L + 128r (r = 0..3) of a slot; item i is
-    // token i >> 4, 16-dim segment i & 15.
+    // + scales -> bf16 rows of a sub-tile buffer (two slots per 64-token
+    // sub-tile, three buffers in turn).  Lane L (0..127) handles items
+    // L + 128r (r = 0..3) of a slot; item i is token i >> 4, 16-dim segment
+    // i & 15.
     // ------------------------------------------------------------------
     const int L = tid - 256;
-    uint32_t n_tile = 0, n_chunk = 0;
+    uint32_t n_tile = 0, n_chunk = 0, n_sub = 0;
     for (int64_t g = span.g_begin; g < span.g_end; ++g, ++n_tile) {
       const uint32_t mp = n_tile & 1;
-      const uint32_t buf = n_tile & 1;
+      mbar_wait(&bars[bSclFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+      const uint8_t* scl = sScl + mp * 1024;
 #pragma unroll 1
-      for (int k = 0; k < 4; ++k, ++n_chunk) {
-        const uint32_t slot = n_chunk % kStgSlots, use = n_chunk / kStgSlots;
-        if (k == 0) {
-          mbar_wait(&bars[bSclFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          if (n_tile >= 2) {
-            mbar_wait(&bars[bKvFree + 2 * buf], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
-            mbar_wait(&bars[bKvFree + 2 * buf + 1], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
-            // Hold the tile stores until the previous tile's S is done, so
-            // that they fall in the softmax phase rather than competing with
-            // that S product for shared-memory bandwidth.  (The phase is
-            // unambiguous: S of this tile cannot complete before these stores.)
-            mbar_wait(&bars[bSFull], (n_tile - 1) & 1, abort_flag, p.d_error, kWaitNs);
-          }
-        }
-        mbar_wait(&bars[bStgFull + slot], use & 1, abort_flag, p.d_error, kWaitNs);
-        const uint8_t* stg = sStg + slot * 8192;
-        const uint8_t* scl = sScl + mp * 1024;
-        uint8_t* tile = sKV + buf * 65536;
+      for (int sub = 0; sub < 2; ++sub, ++n_sub) {
+        const uint32_t buf = n_sub % kKvBufs, use = n_sub / kKvBufs;
+        if (use > 0) mbar_wait(&bars[bKvFree + buf], (use - 1) & 1, abort_flag, p.d_error, kWaitNs);
+        uint8_t* tile = sKV + buf * 32768;
 #pragma unroll 1
-        for (int rb = 0; rb < 4; rb += 2) {
-          uint4 raw[2];
-          uint32_t sb[2];
-          bool big = false;
+        for (int kk = 0; kk < 2; ++kk, ++n_chunk) {
+          const int k = 2 * sub + kk;  // slot of the 128-token tile
+          const uint32_t slot = n_chunk % kStgSlots, suse = n_chunk / kStgSlots;
+          mbar_wait(&bars[bStgFull + slot], suse & 1, abort_flag, p.d_error, kWaitNs);
+          const uint8_t* stg = sStg + slot * 8192;
+#pragma unroll 1
+          for (int rb = 0; rb < 4; rb += 2) {
+            uint4 raw[2];
+            uint32_t sb[2];
+            bool big = false;
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int item = L + 128 * (rb + r);
-            const int tt = item >> 4, s = item & 15;
-            raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
-            const int T = 32 * k + tt;  // scales of token T = 4l + j sit at [j][l]
-            sb[r] = scl[(32 * (T & 3) + (T >> 2)) * 8 + (s >> 1)];
-            big |= sb[r] > 142u;
-          }
-          const bool any_big = __any_sync(0xFFFFFFFFu, big);
+            for (int r = 0; r < 2; ++r) {
+              const int item = L + 128 * (rb + r);
+              const int tt = item >> 4, s = item & 15;
+              raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
+              const int T = 32 * k + tt;  // scales of token T = 4l + j sit at [j][l]
+              sb[r] = scl[(32 * (T & 3) + (T >> 2)) * 8 + (s >> 1)];
+              big |= sb[r] > 142u;
+            }
+            const bool any_big = __any_sync(0xFFFFFFFFu, big);
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int item = L + 128 * (rb + r);
-            const int t = 32 * k + (item >> 4), s = item & 15;
-            uint32_t o[8];
-            if (!any_big)
-              dequant_fp8_16_small_scale(raw[r], sb[r], o);
-            else
-              dequant_fp8_16(raw[r], sb[r], o);
-            uint8_t* chunk = tile + (s >> 2) * 16384;
-            // Segments of odd 64-dim chunks store their upper 16-byte unit
-            // first, so that the 8 lanes of each quarter-warp store to 8
-            // distinct bank groups.
-            const bool odd = (s >> 2) & 1;
-            const int u = 2 * (s & 3);
-            const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
-            *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + odd) * 16)) = odd ? hi : lo;
-            *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + !odd) * 16)) = odd ? lo : hi;
+            for (int r = 0; r < 2; ++r) {
+              const int item = L + 128 * (rb + r);
+              const int t = 32 * kk + (item >> 4), s = item & 15;  // row of the sub-tile
+              uint32_t o[8];
+              if (!any_big)
+                dequant_fp8_16_small_scale(raw[r], sb[r], o);
+              else
+                dequant_fp8_16(raw[r], sb[r], o);
+              uint8_t* chunk = tile + (s >> 2) * 8192;
+              // Segments of odd 64-dim chunks store their upper 16-byte unit
+              // first, so that the 8 lanes of each quarter-warp store to 8
+              // distinct bank groups.
+              const bool odd = (s >> 2) & 1;
+              const int u = 2 * (s & 3);
+              const uint4 lo = make_uint4(o[0], o[1], o[2], o[3]), hi = make_uint4(o[4], o[5], o[6], o[7]);
+              *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + odd) * 16)) = odd ? hi : lo;
+              *reinterpret_cast<uint4*>(chunk + swz<128>(t * 128 + (u + !odd) * 16)) = odd ? lo : hi;
+            }
           }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars[bKvFull + 4 * buf + k]);
-          mbar_arrive(&bars[bStgFree + slot]);
-          if (k == 3) mbar_arrive(&bars[bSclFree + mp]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars[bKvFull + buf]);
+            mbar_arrive(&bars[bStgFree + slot]);
+            if (k == 3) mbar_arrive(&bars[bSclFree + mp]);
+          }
         }
       }
     }
   } else if (warp == kIssueWarp) {
     // ------------------------------------------------------------------
-    // Tensor-core issue (one thread).  Per tile: S = Q K^T (A = Q in TMEM);
-    // O += P V over this CTA's tokens as soon as its P is written, and over
-    // the peer's tokens once the peer's P has landed; the next tile's S
-    // follows at once.
+    // Tensor-core issue (one thread).  Per 64-token sub-tile n: the next
+    // sub-tile's S = Q K^T (A = Q in shared memory, into the other S
+    // buffer) right away, so that it runs during this sub-tile's softmax;
+    // then O += P V over this CTA's token quarter as soon as its P is
+    // written and over the peer's once the peer's P has landed.
     // ------------------------------------------------------------------
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
-      const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
-      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
-      const int mine0 = static_cast<int>(c) * 64, other0 = static_cast<int>(peer) * 64;
-      uint32_t n_tile = 0, n_seg = 0;
+      const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+      const uint32_t tS = tmem + kColS, tO = tmem + kColO;
+      uint32_t n_sub = 0, n_seg = 0;
       bool issued = false;
       auto issue_qk = [&](uint32_t nt) {
-        const uint32_t buf = nt & 1;
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) mbar_wait(&bars[bKvFull + 4 * buf + k], (nt >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+        const uint32_t buf = nt % kKvBufs, sb = nt & 1;
+        if (nt >= 2) mbar_wait(&bars[bSUsed + sb], ((nt - 2) >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+        mbar_wait(&bars[bKvFull + buf], (nt / kKvBufs) & 1, abort_flag, p.d_error, kWaitNs);
         tc_fence_after();
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t b = make_smem_desc(kv_base + buf * 65536 + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
-            mma_bf16_ts(tS, tQ + k * 32 + kk * 8, b, idesc_qk, (k | kk) != 0);
+            const uint64_t a = make_smem_desc(q_base + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
+            const uint64_t b = make_smem_desc(kv_base + buf * 32768 + k * 8192 + kk * 32, 16, 1024, kSwizzle128);
+            mma_bf16_ss(tS + 64 * sb, a, b, idesc_qk, (k | kk) != 0);
           }
         }
-        mma_commit(&bars[bSFull]);
+        mma_commit(&bars[bSFull + sb]);
       };
-      auto issue_pv = [&](uint32_t buf, int t0, bool init, bool release) {
+      // O += P V over the 16-token K steps q0, q0+1 (this CTA's quarter or
+      // the peer's) of sub-tile buffer buf.
+      auto issue_pv = [&](uint32_t buf, int q0, bool init) {
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int ks = t0 / 16 + q;
-            const uint64_t a = make_smem_desc(p_base + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128);
+          for (int q = 0; q < 2; ++q) {
+            const int ks = q0 + q;
+            const uint64_t a = make_smem_desc(p_base + (ks >> 1) * 8192 + (ks & 1) * 32, 16, 512, kSwizzle64);
             const uint64_t b =
-                make_smem_desc(kv_base + buf * 65536 + 2 * hh * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
+                make_smem_desc(kv_base + buf * 32768 + 2 * hh * 8192 + ks * 2048, 8192, 1024, kSwizzle128);
             mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(init && q == 0));
           }
-          if (release) mma_commit(&bars[bKvFree + 2 * buf + hh]);
         }
       };
       for (int64_t g = span.g_begin; g < span.g_end;) {
         const int qidx = static_cast<int>(g / p.T);
         const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-        bool first = true;
-        for (; g < seg_end; ++g, ++n_tile) {
+        const uint32_t seg_subs = static_cast<uint32_t>(2 * (seg_end - g));
+        for (uint32_t j = 0; j < seg_subs; ++j, ++n_sub) {
+          const bool first = j == 0;
           if (first) {
-            // Q of this query token is in TMEM once the softmax warps have
-            // written it (after the previous token's epilogue).
+            // Q of this query token is in shared memory once the softmax
+            // warps have written it (after the previous token's epilogue).
             mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
             tc_fence_after();
-            issue_qk(n_tile);
+            issue_qk(n_sub);
             issued = true;
           }
-          const uint32_t buf = n_tile & 1;
-          mbar_wait(&bars[bPMine], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          if (j + 1 < seg_subs) issue_qk(n_sub + 1);
+          const uint32_t buf = n_sub % kKvBufs;
+          mbar_wait(&bars[bPMine], n_sub & 1, abort_flag, p.d_error, kWaitNs);
           tc_fence_after();
-          issue_pv(buf, mine0, first, false);
-          mbar_wait(&bars[bPIn], n_tile & 1, abort_flag, p.d_error, kWaitNs);
+          issue_pv(buf, 2 * static_cast<int>(c), first);
+          mbar_wait(&bars[bPIn], n_sub & 1, abort_flag, p.d_error, kWaitNs);
           tc_fence_after();
-          issue_pv(buf, other0, false, true);
-          if (g + 1 == seg_end) mma_commit(&bars[bOReady]);
-          // The next tile of the same query token: its S right behind this PV.
-          if (g + 1 < seg_end) issue_qk(n_tile + 1);
-          first = false;
+          issue_pv(buf, 2 * static_cast<int>(peer), false);
+          mma_commit(&bars[bKvFree + buf]);
+          mma_commit(&bars[bPvDone]);
+          if (j + 1 == seg_subs) mma_commit(&bars[bOReady]);
         }
+        g = seg_end;
         ++n_seg;
       }
       if (issued) {
@@ -487,25 +475,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   } else {
     // ------------------------------------------------------------------
     // Softmax warps 0-7.  Warp w serves the 32 heads of TMEM lane quadrant
-    // qd = w & 3 (lane <-> head 32 qd + lane <-> TMEM lane) and token columns
-    // 32 ch .. 32 ch + 31 (ch = w >> 2) of each 64-token half, so two warps
-    // share each head.  This CTA owns the softmax of token half c of every
-    // tile: each warp sends its columns of the other half's partial scores to
-    // the peer's same warp and receives the peer's for its columns of this
-    // half; the per-head tile maxima of both warps of a quadrant are swapped
+    // qd = w & 3 (lane <-> head 32 qd + lane <-> TMEM lane) and 16 of the 32
+    // tokens of each quarter (ch = w >> 2), so two warps share each head.
+    // This CTA owns the softmax of quarter c of every sub-tile: each warp
+    // sends its 16 columns of the peer's quarter of the partial scores to the
+    // peer's same warp and receives the peer's for its columns of this
+    // quarter; per-head tile maxima of both warps of a quadrant are swapped
     // with the peer so both CTAs keep identical running maxima; each
     // quadrant's P rows travel to the peer, so both hold all of P for PV.
     // ------------------------------------------------------------------
     const int qd = warp & 3, ch = warp >> 2;
     const int i = 32 * qd + lane;  // head
     const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-    const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO, tQ = tmem + lane_base + kColQ;
+    const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO;
     // Staging block of this warp = rows 32 qd .. 32 qd + 31 of P chunk ch;
     // the quadrant's P rows of this CTA's chunk are the block of warp (qd, c).
-    const uint32_t stg_off = ch * 16384 + qd * 4096;
-    const int mine0 = static_cast<int>(c) * 64, other0 = static_cast<int>(peer) * 64;
+    const uint32_t stg_off = ch * 8192 + qd * 2048;
     const int pair_bar = 2 + qd;  // named barrier of the two warps of quadrant qd
-    uint32_t n_tile = 0, n_seg = 0;
+    uint32_t n_tile = 0, n_sub = 0, n_seg = 0;
     float m = -INFINITY, l = 0.f;  // running max (shared by both CTAs) and this warp's part of the row sum
     for (int64_t g = span.g_begin; g < span.g_end;) {
       const int qidx = static_cast<int>(g / p.T);
@@ -513,186 +500,196 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int64_t seg_begin = g;
       if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bStatsIn + (n_seg & 1)], 1024);
       {
-        // Q row i, dims [128 ch, 128 ch + 128) of my half, into TMEM as packed
-        // bf16 pairs.
+        // Q row i, dims [128 ch, 128 ch + 128) of my half, into shared
+        // memory as the K-major A operand (chunks 2 ch, 2 ch + 1).
         const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qidx) * kHeads + i) * kD +
                                                           static_cast<int>(c) * kHalf + ch * 128);
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          uint32_t v[32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 w = __ldg(src + j * 8 + u);
-            v[4 * u] = w.x;
-            v[4 * u + 1] = w.y;
-            v[4 * u + 2] = w.z;
-            v[4 * u + 3] = w.w;
-          }
-          tmem_st32(tQ + 64 * ch + 32 * j, v);
+        for (int j = 0; j < 2; ++j) {
+          uint4 w[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) w[u] = __ldg(src + j * 8 + u);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(sQ + (2 * ch + j) * 16384 + swz<128>(i * 128 + u * 16)) = w[u];
         }
-        tmem_wait_st();
-        tc_fence_before();
+        fence_proxy_async_smem();
         mbar_arrive(&bars[bQFull]);
       }
       for (; g < seg_end; ++g, ++n_tile) {
-        if (lane == 0) {
-          mbar_expect_tx(&bars[bXFull + warp], kXWarpBytes);
-          if (ch == 0) mbar_expect_tx(&bars[bMaxFull + qd], 256);
-        }
-        mbar_wait(&bars[bSFull], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        // The previous tile's P from the peer has landed (this S follows the
-        // PV that waited for it), so the P barrier is in its next phase.
-        if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
-        // This warp's copies of the previous tile out of its block are read.
-        if (lane == 0) bulk_wait_read();
-        __syncwarp();
-        tc_fence_after();
-        // 1. My columns of the other half's partial scores, pre-scaled, to my
-        //    staging block (free: this CTA's PV of the previous tile is done)
-        //    and on to the peer's same warp.
-        {
-          uint32_t v[32];
-          tmem_ld32(tS + other0 + 32 * ch, v);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(sP + stg_off + lane * 128 + ((u ^ (lane & 7)) << 4)) =
-                make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
-                           __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
-                           __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
-                           __float_as_uint(__uint_as_float(v[4 * u + 3]) * p.scale_log2));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          // The peer's X block of this warp is free: this CTA has received
-          // the peer's P of the previous tile (this S follows the PV that
-          // waited for it), which the peer sent after its warps read X.
-          bulk_to_peer(peer_of(smem_u32(sX + warp * 4096), peer), sP + stg_off, kXWarpBytes,
-                       peer_of(smem_u32(&bars[bXFull + warp]), peer));
-          bulk_commit();
-        }
-        // 2. One pass over my columns of my token half: y = scaled S + X
-        //    (-inf where masked), kept in TMEM; P against the running maximum
-        //    of the earlier tiles into my P units; its row sum; the maximum.
+        // Validity of the 128-token tile: bit b of word e covers token 4b + e.
         const uint32_t mp = n_tile & 1;
         mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-        // Validity of my token mine0 + 32 ch + 4u + e is bit 8e + u of mk.
-        uint32_t mk = 0;
+        uint32_t mkw[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) mk |= ((sMask[mp * 4 + e] >> (16 * c + 8 * ch)) & 0xFFu) << (8 * e);
+        for (int e = 0; e < 4; ++e) mkw[e] = sMask[mp * 4 + e];
         mbar_arrive(&bars[bMaskFree + mp]);
-        mbar_wait(&bars[bXFull + warp], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        // My P units sit in the staging block of warp (qd, c): both warps'
-        // staging copies must have been read.
-        if (lane == 0) bulk_wait_read();
-        named_bar_sync(pair_bar, 64);
-        float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          uint32_t v[32];
-          tmem_ld32(tS + mine0 + 32 * ch, v);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float4 x4 =
-                *reinterpret_cast<const float4*>(sX + warp * 4096 + lane * 128 + ((u ^ (lane & 7)) << 4));
-            const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const bool ok = (mk >> (8 * e + u)) & 1u;
-              const float y = ok ? fmaf(__uint_as_float(v[4 * u + e]), p.scale_log2, xs[e]) : -INFINITY;
-              mx[e] = fmaxf(mx[e], y);
-              v[4 * u + e] = __float_as_uint(y);
-            }
-          }
-          tmem_st32(tS + mine0 + 32 * ch, v);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
-              ls[e & 3] += pv[e];
-            }
-            *reinterpret_cast<uint4*>(sP + c * 16384 + swz<128>(i * 128 + (4 * ch + w) * 16)) =
-                make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                           pack_bf16x2(pv[6], pv[7]));
-          }
-        }
-        const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        tmem_wait_st();
-        // 3. Swap tile maxima: this warp's 32 with the peer's same warp; the
-        //    quadrant's four per head (two warps, two CTAs) decide alike in
-        //    both CTAs and both warps.
-        sMaxOut[64 * qd + 32 * ch + lane] = mloc;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          bulk_to_peer(peer_of(smem_u32(sMaxIn + 64 * qd + 32 * ch), peer), sMaxOut + 64 * qd + 32 * ch, 128,
-                       peer_of(smem_u32(&bars[bMaxFull + qd]), peer));
-          bulk_commit();
-        }
-        named_bar_sync(pair_bar, 64);  // the partner warp's maxima are in place
-        mbar_wait(&bars[bMaxFull + qd], n_tile & 1, abort_flag, p.d_error, kWaitNs);
-        const float mt = fmaxf(fmaxf(sMaxOut[64 * qd + lane], sMaxOut[64 * qd + 32 + lane]),
-                               fmaxf(sMaxIn[64 * qd + lane], sMaxIn[64 * qd + 32 + lane]));
-        const bool need = mt > m + kLazy || (m == -INFINITY && mt > -INFINITY);
-        float alpha = 1.f;
-        if (!__any_sync(0xFFFFFFFFu, need)) {
-          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-        } else {
-          // Rare (the first tile, or a head's maximum grew by more than the
-          // lazy threshold): move the running maximum, rescale the row sum
-          // (and below, my O columns), and recompute my P units from y.
-          if (need) {
-            alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
-            m = mt;
-          }
-          l *= alpha;
-          mm = m == -INFINITY ? 0.f : m;
-          float lr[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t v[32];
-          tmem_ld32(tS + mine0 + 32 * ch, v);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
-              lr[e & 3] += pv[e];
-            }
-            *reinterpret_cast<uint4*>(sP + c * 16384 + swz<128>(i * 128 + (4 * ch + w) * 16)) =
-                make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                           pack_bf16x2(pv[6], pv[7]));
-          }
-          l += (lr[0] + lr[1]) + (lr[2] + lr[3]);
-        }
-        // alpha == 0 only while m was -inf: O then holds zeros (every P so
-        // far was 0) or, on a segment's first tile, values that this tile's
-        // PV overwrites; either way nothing needs scaling.
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.f && alpha != 0.f)) {
 #pragma unroll 1
-          for (int j = 0; j < 8; ++j) {
-            uint32_t o[16];
-            tmem_ld16(tO + 128 * ch + 16 * j, o);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st16(tO + 128 * ch + 16 * j, o);
+        for (int sub = 0; sub < 2; ++sub, ++n_sub) {
+          const uint32_t sb = n_sub & 1;
+          const uint32_t tSb = tS + 64 * sb;
+          if (lane == 0) {
+            mbar_expect_tx(&bars[bXFull + warp], kXWarpBytes);
+            if (ch == 0) mbar_expect_tx(&bars[bMaxFull + qd], 256);
           }
+          mbar_wait(&bars[bSFull + sb], (n_sub >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+          // The previous sub-tile's PV is done: the P buffer (this sub-tile's
+          // staging) is free, and the peer's P of that sub-tile has landed,
+          // so the P barrier is in its next phase.
+          if (n_sub > 0) mbar_wait(&bars[bPvDone], (n_sub - 1) & 1, abort_flag, p.d_error, kWaitNs);
+          if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
+          // This warp's copies of the previous sub-tile out of its block are read.
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+          tc_fence_after();
+          // 1. My 16 columns of the peer's quarter of the partial scores,
+          //    pre-scaled, to my staging block and on to the peer's same warp.
+          {
+            uint32_t v[16];
+            tmem_ld16(tSb + 32 * peer + 16 * ch, v);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(sP + stg_off + swz<64>(lane * 64 + u * 16)) =
+                  make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
+                             __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
+                             __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
+                             __float_as_uint(__uint_as_float(v[4 * u + 3]) * p.scale_log2));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // The peer's X block of this warp is free: this CTA has received
+            // the peer's P of the previous sub-tile (its PV, waited above,
+            // needed it), which the peer sent after its warps read X.
+            bulk_to_peer(peer_of(smem_u32(sX + warp * 2048), peer), sP + stg_off, kXWarpBytes,
+                         peer_of(smem_u32(&bars[bXFull + warp]), peer));
+            bulk_commit();
+          }
+          // 2. My 16 columns of my quarter: y = scaled S + X (-inf where
+          //    masked), kept in TMEM; P against the running maximum of the
+          //    earlier tiles into my P units; its row sum; the tile maximum.
+          uint32_t mk = 0;  // bit 4e + u: token 32c + 16ch + 4u + e of this sub-tile
+          {
+            const int shift = 16 * sub + 8 * static_cast<int>(c) + 4 * ch;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mk |= ((mkw[e] >> shift) & 0xFu) << (4 * e);
+          }
+          mbar_wait(&bars[bXFull + warp], (n_sub & 1), abort_flag, p.d_error, kWaitNs);
+          // My P units sit in the staging block of warp (qd, c): both warps'
+          // staging copies must have been read.
+          if (lane == 0) bulk_wait_read();
+          named_bar_sync(pair_bar, 64);
+          const float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            uint32_t v[16];
+            tmem_ld16(tSb + 32 * c + 16 * ch, v);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float4 x4 = *reinterpret_cast<const float4*>(sX + warp * 2048 + swz<64>(lane * 64 + u * 16));
+              const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const bool ok = (mk >> (4 * e + u)) & 1u;
+                const float y = ok ? fmaf(__uint_as_float(v[4 * u + e]), p.scale_log2, xs[e]) : -INFINITY;
+                mx[e] = fmaxf(mx[e], y);
+                v[4 * u + e] = __float_as_uint(y);
+              }
+            }
+            tmem_st16(tSb + 32 * c + 16 * ch, v);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              float pv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
+                ls[e & 3] += pv[e];
+              }
+              *reinterpret_cast<uint4*>(sP + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
+                  make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                             pack_bf16x2(pv[6], pv[7]));
+            }
+          }
+          const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           tmem_wait_st();
-        }
-        // 4. The quadrant's P rows to the peer, from the warp whose staging
-        //    block holds them (so its own wait covers the copy's reads).
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bars[bPMine]);  // the tensor core may start on this CTA's tokens
-        named_bar_sync(pair_bar, 64);
-        if (ch == static_cast<int>(c) && lane == 0) {
-          // The peer's block for these rows is free: the peer's warps sent
-          // this tile's X from it after its previous PV had completed.
-          bulk_to_peer(peer_of(smem_u32(sP + c * 16384 + qd * 4096), peer), sP + c * 16384 + qd * 4096, 4096,
-                       peer_of(smem_u32(&bars[bPIn]), peer));
-          bulk_commit();
+          // 3. Swap tile maxima: this warp's 32 with the peer's same warp; the
+          //    quadrant's four per head (two warps, two CTAs) decide alike in
+          //    both CTAs and both warps.
+          sMaxOut[64 * qd + 32 * ch + lane] = mloc;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            bulk_to_peer(peer_of(smem_u32(sMaxIn + 64 * qd + 32 * ch), peer), sMaxOut + 64 * qd + 32 * ch, 128,
+                         peer_of(smem_u32(&bars[bMaxFull + qd]), peer));
+            bulk_commit();
+          }
+          named_bar_sync(pair_bar, 64);  // the partner warp's maxima are in place
+          mbar_wait(&bars[bMaxFull + qd], n_sub & 1, abort_flag, p.d_error, kWaitNs);
+          const float mt = fmaxf(fmaxf(sMaxOut[64 * qd + lane], sMaxOut[64 * qd + 32 + lane]),
+                                 fmaxf(sMaxIn[64 * qd + lane], sMaxIn[64 * qd + 32 + lane]));
+          const bool need = mt > m + kLazy || (m == -INFINITY && mt > -INFINITY);
+          float alpha = 1.f;
+          if (!__any_sync(0xFFFFFFFFu, need)) {
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          } else {
+            // Rare (a segment's first sub-tile, or a head's maximum grew by
+            // more than the lazy threshold): move the running maximum,
+            // rescale the row sum (and below, my O columns), and recompute
+            // my P units from y.
+            if (need) {
+              alpha = m == -INFINITY ? 0.f : ex2_approx(m - mt);
+              m = mt;
+            }
+            l *= alpha;
+            const float mm2 = m == -INFINITY ? 0.f : m;
+            float lr[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t v[16];
+            tmem_ld16(tSb + 32 * c + 16 * ch, v);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              float pv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm2);
+                lr[e & 3] += pv[e];
+              }
+              *reinterpret_cast<uint4*>(sP + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
+                  make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                             pack_bf16x2(pv[6], pv[7]));
+            }
+            l += (lr[0] + lr[1]) + (lr[2] + lr[3]);
+          }
+          // S of this sub-tile has been read for the last time.
+          tc_fence_before();
+          mbar_arrive(&bars[bSUsed + sb]);
+          // alpha == 0 only while m was -inf: O then holds zeros (every P so
+          // far was 0) or, on a segment's first sub-tile, values that this
+          // sub-tile's PV overwrites; either way nothing needs scaling.
+          if (__any_sync(0xFFFFFFFFu, alpha != 1.f && alpha != 0.f)) {
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {
+              uint32_t o[16];
+              tmem_ld16(tO + 128 * ch + 16 * j, o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st16(tO + 128 * ch + 16 * j, o);
+            }
+            tmem_wait_st();
+          }
+          // 4. The quadrant's P rows to the peer, from the warp whose staging
+          //    block holds them (so its own wait covers the copy's reads).
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&bars[bPMine]);  // the tensor core may start on this CTA's tokens
+          named_bar_sync(pair_bar, 64);
+          if (ch == static_cast<int>(c) && lane == 0) {
+            // The peer's block for these rows is free: the peer's warps sent
+            // this sub-tile's X from it after its previous PV had completed.
+            bulk_to_peer(peer_of(smem_u32(sP + c * 8192 + qd * 2048), peer), sP + c * 8192 + qd * 2048,
+                         kPQuadBytes, peer_of(smem_u32(&bars[bPIn]), peer));
+            bulk_commit();
+          }
         }
       }
 
