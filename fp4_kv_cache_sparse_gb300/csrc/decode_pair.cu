@@ -7,21 +7,25 @@
 // it"), for an FP8 main cache without an extra cache.  The layout differs:
 // heads are the MMA's M dimension (all 128 of them).  O for 128 heads x 512
 // dims would fill all of TMEM, so CTA c of the pair owns dims [256c, 256c+256):
-// its half of every record, of Q, of the bf16 tile and of O.  Each CTA's S is
-// a partial sum over its dims.  A scheduled 128-token tile is processed as two
-// 64-token sub-tiles, so that S fits TMEM twice: the tensor core computes the
-// next sub-tile's S = Q K^T (Q in shared memory) while the softmax warps work
-// on the current one.  CTA c computes the softmax of token quarter c of every
-// sub-tile (tokens 32c .. 32c+31) for all heads: it sends the peer its
-// partial scores of the peer's quarter and receives the peer's for its own
-// (bulk asynchronous copies between the two shared memories, completing on
-// the receiver's mbarrier), the two CTAs swap per-head tile maxima so that
-// they keep identical running maxima (and rescale factors), and each sends
-// the other its part of P, so both hold all of P for their O += P V.  The
-// bf16 tile is triple-buffered; records reach shared memory by TMA row
-// gathers (tile::gather4, 4 tokens per instruction, 256 bytes of a record per
-// row) into a 3-slot staging ring, so the dequantizing warps never have
-// global loads in flight when they publish a slot.
+// its half of every record, of Q (kept in TMEM as the A operand of
+// S = Q K^T), of the bf16 tile and of O.  Each CTA's S is a partial sum over
+// its dims.  A scheduled 128-token tile is processed as two 64-token
+// sub-tiles, so that S fits TMEM twice next to O and Q: the tensor core
+// computes the next sub-tile's S while the softmax warps work on the current
+// one.  CTA c computes the softmax of token quarter c of every sub-tile
+// (tokens 32c .. 32c+31) for all heads: it sends the peer its partial scores
+// of the peer's quarter and receives the peer's for its own (bulk
+// asynchronous copies between the two shared memories, completing on the
+// receiver's mbarrier), the two CTAs swap per-head tile maxima so that they
+// keep identical running maxima (and rescale factors), and each sends the
+// other its part of P, so both hold all of P for their O += P V.  P and the
+// received partial scores are double-buffered by sub-tile parity, so a
+// sub-tile's softmax does not wait for the previous sub-tile's PV; the bf16
+// tile is triple-buffered.  One thread issues each product as soon as its
+// inputs are ready.  Records reach shared memory by TMA row gathers
+// (tile::gather4, 4 tokens per instruction, 256 bytes of a record per row)
+// into a 3-slot staging ring, so the dequantizing warps never have global
+// loads in flight when they publish a slot.
 //
 // Warps: 0-7 softmax (two per TMEM lane quadrant, one per 16-token column
 // half of the quarter), 8-11 dequant, 12 loader (indices, validity mask,
@@ -52,12 +56,13 @@ constexpr uint32_t kPQuadBytes = 32 * 64;       // a quadrant's 32 heads x 32 to
 constexpr uint32_t kPInBytes = 4 * kPQuadBytes;  // the peer's quarter of P
 
 struct PairSmem {
-  static constexpr int kQ = 0;                   // Q: 4 chunks x [128 heads x 128 B] bf16 (this CTA's dims), SW128
-  static constexpr int kKV = kQ + 65536;         // 3 buffers x 4 chunks x [64 tokens x 128 B], SW128
-  static constexpr int kP = kKV + kKvBufs * 32768;  // 2 chunks (32 tokens each) x [128 heads x 64 B] bf16, SW64;
-                                                 // also the outgoing staging of the partial scores
-  static constexpr int kX = kP + 16384;          // 8 warps x [32 heads x 16 tokens] fp32 from the peer, SW64 units
-  static constexpr int kStg = kX + 16384;        // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
+  static constexpr int kKV = 0;                  // 3 buffers x 4 chunks x [64 tokens x 128 B], SW128
+  static constexpr int kP = kKV + kKvBufs * 32768;  // 2 buffers (sub-tile parity) x 2 chunks (32 tokens each)
+                                                 // x [128 heads x 64 B] bf16, SW64; also the outgoing staging
+                                                 // of the partial scores
+  static constexpr int kX = kP + 2 * 16384;      // 2 buffers x 8 warps x [32 heads x 16 tokens] fp32 from the
+                                                 // peer, SW64 units
+  static constexpr int kStg = kX + 2 * 16384;    // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
   static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [4][32] x 8 B e8m0 scales of this CTA's dims
                                                         // (token 4l + j of a 128-token tile at [j][l])
   static constexpr int kBar = kScl + 2 * 1024;   // 64 mbarriers
@@ -74,12 +79,15 @@ struct PairSmem {
 enum PairBar {
   bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
   bKvFull = 14 /* [3 buffers] */, bKvFree = 17 /* [3] */, bQFull = 20, bSFull = 21 /* [2 S buffers] */,
-  bSUsed = 23 /* [2] */, bPMine = 25, bPIn = 26, bPvDone = 27, bOReady = 28, bStatsIn = 29 /* [2] */, bDrain = 31,
-  bXFull = 32 /* [8 warps] */, bMaxFull = 40 /* [4 quadrants] */
+  bSUsed = 23 /* [2] */, bPMine2 = 25 /* [2] by sub-tile parity */, bPIn = 27 /* [2 P buffers] */,
+  bPvDone = 29 /* [2] */, bOReady = 31, bStatsIn = 32 /* [2] */, bDrain = 34,
+  bXFull = 35 /* [2 X buffers][8 warps] */, bMaxFull = 51 /* [4 quadrants] */
 };
 
-// TMEM columns: S [0, 128) as two 64-column buffers, O [128, 384).
-constexpr uint32_t kColS = 0, kColO = 128;
+// TMEM columns: S [0, 128) as two 64-column buffers, O [128, 384), Q [384, 512)
+// (this CTA's 256 dims of the query token as packed bf16 pairs: the A operand
+// of S = Q K^T).
+constexpr uint32_t kColS = 0, kColO = 128, kColQ = 384;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -108,6 +116,19 @@ __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Non-blocking test of a phase's completion.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
@@ -122,6 +143,18 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
       "%5, %6}], [%7];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M rows (lanes) x K
+// columns of packed bf16 pairs.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -179,7 +212,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   using L = PairSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + L::kQ;
   uint8_t* sKV = smem + L::kKV;
   uint8_t* sP = smem + L::kP;
   uint8_t* sX = smem + L::kX;
@@ -220,12 +252,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bars[bKvFree + b], 1);
     }
     mbar_init(&bars[bQFull], kSoftThreads);
-    mbar_init(&bars[bPMine], kSoftThreads);
-    mbar_init(&bars[bPIn], 1);
-    mbar_init(&bars[bPvDone], 1);
+    for (int b = 0; b < 2; ++b) mbar_init(&bars[bPMine2 + b], kSoftThreads);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[bPIn + b], 1);
+      mbar_init(&bars[bPvDone + b], 1);
+    }
     mbar_init(&bars[bOReady], 1);
     mbar_init(&bars[bDrain], 1);
-    for (int w = 0; w < 8; ++w) mbar_init(&bars[bXFull + w], 1);
+    for (int w = 0; w < 16; ++w) mbar_init(&bars[bXFull + w], 1);
     for (int w = 0; w < 4; ++w) mbar_init(&bars[bMaxFull + w], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -393,44 +427,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
   } else if (warp == kIssueWarp) {
     // ------------------------------------------------------------------
-    // Tensor-core issue (one thread).  Per 64-token sub-tile n: the next
-    // sub-tile's S = Q K^T (A = Q in shared memory, into the other S
-    // buffer) right away, so that it runs during this sub-tile's softmax;
-    // then O += P V over this CTA's token quarter as soon as its P is
-    // written and over the peer's once the peer's P has landed.
+    // Tensor-core issue (one thread): per 64-token sub-tile, S = Q K^T
+    // (A = Q in shared memory, into the S buffer of the sub-tile's parity),
+    // O += P V over this CTA's token quarter once its P is written and over
+    // the peer's once the peer's P has landed, each as soon as it can go.
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
-      const uint32_t q_base = smem_u32(sQ), kv_base = smem_u32(sKV), p_base = smem_u32(sP);
-      const uint32_t tS = tmem + kColS, tO = tmem + kColO;
+      const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
       uint32_t n_sub = 0, n_seg = 0;
       bool issued = false;
       auto issue_qk = [&](uint32_t nt) {
         const uint32_t buf = nt % kKvBufs, sb = nt & 1;
-        if (nt >= 2) mbar_wait(&bars[bSUsed + sb], ((nt - 2) >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-        mbar_wait(&bars[bKvFull + buf], (nt / kKvBufs) & 1, abort_flag, p.d_error, kWaitNs);
-        tc_fence_after();
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = make_smem_desc(q_base + k * 16384 + kk * 32, 16, 1024, kSwizzle128);
             const uint64_t b = make_smem_desc(kv_base + buf * 32768 + k * 8192 + kk * 32, 16, 1024, kSwizzle128);
-            mma_bf16_ss(tS + 64 * sb, a, b, idesc_qk, (k | kk) != 0);
+            mma_bf16_ts(tS + 64 * sb, tQ + k * 32 + kk * 8, b, idesc_qk, (k | kk) != 0);
           }
         }
         mma_commit(&bars[bSFull + sb]);
       };
       // O += P V over the 16-token K steps q0, q0+1 (this CTA's quarter or
       // the peer's) of sub-tile buffer buf.
-      auto issue_pv = [&](uint32_t buf, int q0, bool init) {
+      auto issue_pv = [&](uint32_t buf, uint32_t pb, int q0, bool init) {
 #pragma unroll 1
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int ks = q0 + q;
-            const uint64_t a = make_smem_desc(p_base + (ks >> 1) * 8192 + (ks & 1) * 32, 16, 512, kSwizzle64);
+            const uint64_t a =
+                make_smem_desc(p_base + pb * 16384 + (ks >> 1) * 8192 + (ks & 1) * 32, 16, 512, kSwizzle64);
             const uint64_t b =
                 make_smem_desc(kv_base + buf * 32768 + 2 * hh * 8192 + ks * 2048, 8192, 1024, kSwizzle128);
             mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(init && q == 0));
@@ -441,28 +471,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const int qidx = static_cast<int>(g / p.T);
         const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
         const uint32_t seg_subs = static_cast<uint32_t>(2 * (seg_end - g));
-        for (uint32_t j = 0; j < seg_subs; ++j, ++n_sub) {
-          const bool first = j == 0;
-          if (first) {
-            // Q of this query token is in shared memory once the softmax
-            // warps have written it (after the previous token's epilogue).
-            mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
-            tc_fence_after();
-            issue_qk(n_sub);
-            issued = true;
+        const uint32_t base = n_sub;
+        // Q of this query token is in shared memory once the softmax warps
+        // have written it (after the previous token's epilogue).
+        mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
+        tc_fence_after();
+        issued = true;
+        // Issue each product of the segment as soon as its inputs are ready:
+        // the second half of O += P V first (it frees a tile buffer for the
+        // dequantizers), then the first half, then the next S = Q K^T (its S
+        // buffer released by the softmax two sub-tiles back, its tile in
+        // shared memory), so that the tensor core works during the softmax.
+        uint32_t qk = 0, pva = 0, pvb = 0;
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 0; pvb < seg_subs; ++it) {
+          bool progress = false;
+          if (pvb < pva) {
+            const uint32_t n = base + pvb, pb = n & 1;
+            if (mbar_test(&bars[bPIn + pb], (n >> 1) & 1)) {
+              tc_fence_after();
+              issue_pv(n % kKvBufs, pb, 2 * static_cast<int>(peer), false);
+              mma_commit(&bars[bKvFree + n % kKvBufs]);
+              mma_commit(&bars[bPvDone + pb]);
+              if (pvb + 1 == seg_subs) mma_commit(&bars[bOReady]);
+              ++pvb;
+              progress = true;
+            }
           }
-          if (j + 1 < seg_subs) issue_qk(n_sub + 1);
-          const uint32_t buf = n_sub % kKvBufs;
-          mbar_wait(&bars[bPMine], n_sub & 1, abort_flag, p.d_error, kWaitNs);
-          tc_fence_after();
-          issue_pv(buf, 2 * static_cast<int>(c), first);
-          mbar_wait(&bars[bPIn], n_sub & 1, abort_flag, p.d_error, kWaitNs);
-          tc_fence_after();
-          issue_pv(buf, 2 * static_cast<int>(peer), false);
-          mma_commit(&bars[bKvFree + buf]);
-          mma_commit(&bars[bPvDone]);
-          if (j + 1 == seg_subs) mma_commit(&bars[bOReady]);
+          if (pva < qk) {
+            const uint32_t n = base + pva;
+            if (mbar_test(&bars[bPMine2 + (n & 1)], (n >> 1) & 1)) {
+              tc_fence_after();
+              issue_pv(n % kKvBufs, n & 1, 2 * static_cast<int>(c), pva == 0);
+              ++pva;
+              progress = true;
+            }
+          }
+          if (qk < seg_subs && qk < pva + 2) {
+            const uint32_t n = base + qk, buf = n % kKvBufs;
+            if ((n < 2 || mbar_test(&bars[bSUsed + (n & 1)], ((n - 2) >> 1) & 1)) &&
+                mbar_test(&bars[bKvFull + buf], (n / kKvBufs) & 1)) {
+              tc_fence_after();
+              issue_qk(n);
+              ++qk;
+              progress = true;
+            }
+          }
+          if (!progress) {
+            __nanosleep(32);
+            if ((it & 63) == 63) {
+              if (*abort_flag) break;
+              if (global_timer_ns() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                if (p.d_error) atomicOr(p.d_error, MLA_DEVERR_TIMEOUT);
+                break;
+              }
+            }
+          }
         }
+        n_sub = base + seg_subs;
         g = seg_end;
         ++n_seg;
       }
@@ -487,9 +554,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int qd = warp & 3, ch = warp >> 2;
     const int i = 32 * qd + lane;  // head
     const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-    const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO;
-    // Staging block of this warp = rows 32 qd .. 32 qd + 31 of P chunk ch;
-    // the quadrant's P rows of this CTA's chunk are the block of warp (qd, c).
+    const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO, tQ = tmem + lane_base + kColQ;
+    // Staging block of this warp = rows 32 qd .. 32 qd + 31 of chunk ch of
+    // the sub-tile's P buffer; the quadrant's P rows of this CTA's chunk are
+    // the block of warp (qd, c).
     const uint32_t stg_off = ch * 8192 + qd * 2048;
     const int pair_bar = 2 + qd;  // named barrier of the two warps of quadrant qd
     uint32_t n_tile = 0, n_sub = 0, n_seg = 0;
@@ -500,20 +568,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int64_t seg_begin = g;
       if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bStatsIn + (n_seg & 1)], 1024);
       {
-        // Q row i, dims [128 ch, 128 ch + 128) of my half, into shared
-        // memory as the K-major A operand (chunks 2 ch, 2 ch + 1).
+        // Q row i, dims [128 ch, 128 ch + 128) of my half, into TMEM as
+        // packed bf16 pairs (columns 64 ch .. 64 ch + 63 of the Q area).
         const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qidx) * kHeads + i) * kD +
                                                           static_cast<int>(c) * kHalf + ch * 128);
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < 2; ++j) {
-          uint4 w[8];
+          uint32_t v[32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) w[u] = __ldg(src + j * 8 + u);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(sQ + (2 * ch + j) * 16384 + swz<128>(i * 128 + u * 16)) = w[u];
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = __ldg(src + j * 8 + u);
+            v[4 * u] = w.x;
+            v[4 * u + 1] = w.y;
+            v[4 * u + 2] = w.z;
+            v[4 * u + 3] = w.w;
+          }
+          tmem_st32(tQ + 64 * ch + 32 * j, v);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
         mbar_arrive(&bars[bQFull]);
       }
       for (; g < seg_end; ++g, ++n_tile) {
@@ -526,18 +599,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         mbar_arrive(&bars[bMaskFree + mp]);
 #pragma unroll 1
         for (int sub = 0; sub < 2; ++sub, ++n_sub) {
-          const uint32_t sb = n_sub & 1;
+          const uint32_t sb = n_sub & 1, pb = n_sub & 1;  // S, P and X buffers of this sub-tile
           const uint32_t tSb = tS + 64 * sb;
+          uint8_t* sPb = sP + pb * 16384;
+          const uint8_t* sXw = sX + pb * 16384 + warp * 2048;
           if (lane == 0) {
-            mbar_expect_tx(&bars[bXFull + warp], kXWarpBytes);
+            mbar_expect_tx(&bars[bXFull + 8 * pb + warp], kXWarpBytes);
             if (ch == 0) mbar_expect_tx(&bars[bMaxFull + qd], 256);
           }
           mbar_wait(&bars[bSFull + sb], (n_sub >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          // The previous sub-tile's PV is done: the P buffer (this sub-tile's
-          // staging) is free, and the peer's P of that sub-tile has landed,
-          // so the P barrier is in its next phase.
-          if (n_sub > 0) mbar_wait(&bars[bPvDone], (n_sub - 1) & 1, abort_flag, p.d_error, kWaitNs);
-          if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn], kPInBytes);
+          // The PV of two sub-tiles back is done: this P buffer (and this
+          // sub-tile's staging) is free, and the peer's P of that sub-tile
+          // has landed, so this P barrier is in its next phase.
+          if (n_sub >= 2) mbar_wait(&bars[bPvDone + pb], ((n_sub - 2) >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+          if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn + pb], kPInBytes);
           // This warp's copies of the previous sub-tile out of its block are read.
           if (lane == 0) bulk_wait_read();
           __syncwarp();
@@ -549,7 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             tmem_ld16(tSb + 32 * peer + 16 * ch, v);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(sP + stg_off + swz<64>(lane * 64 + u * 16)) =
+              *reinterpret_cast<uint4*>(sPb + stg_off + swz<64>(lane * 64 + u * 16)) =
                   make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
                              __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
                              __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
@@ -558,11 +633,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            // The peer's X block of this warp is free: this CTA has received
-            // the peer's P of the previous sub-tile (its PV, waited above,
-            // needed it), which the peer sent after its warps read X.
-            bulk_to_peer(peer_of(smem_u32(sX + warp * 2048), peer), sP + stg_off, kXWarpBytes,
-                         peer_of(smem_u32(&bars[bXFull + warp]), peer));
+            // The peer's X block of this warp and parity is free: this CTA
+            // has received the peer's P of two sub-tiles back (its PV,
+            // waited above, needed it), which the peer sent after its warps
+            // read that X.
+            bulk_to_peer(peer_of(smem_u32(sXw), peer), sPb + stg_off, kXWarpBytes,
+                         peer_of(smem_u32(&bars[bXFull + 8 * pb + warp]), peer));
             bulk_commit();
           }
           // 2. My 16 columns of my quarter: y = scaled S + X (-inf where
@@ -574,7 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) mk |= ((mkw[e] >> shift) & 0xFu) << (4 * e);
           }
-          mbar_wait(&bars[bXFull + warp], (n_sub & 1), abort_flag, p.d_error, kWaitNs);
+          mbar_wait(&bars[bXFull + 8 * pb + warp], (n_sub >> 1) & 1, abort_flag, p.d_error, kWaitNs);
           // My P units sit in the staging block of warp (qd, c): both warps'
           // staging copies must have been read.
           if (lane == 0) bulk_wait_read();
@@ -587,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             tmem_ld16(tSb + 32 * c + 16 * ch, v);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float4 x4 = *reinterpret_cast<const float4*>(sX + warp * 2048 + swz<64>(lane * 64 + u * 16));
+              const float4 x4 = *reinterpret_cast<const float4*>(sXw + swz<64>(lane * 64 + u * 16));
               const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -606,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
                 ls[e & 3] += pv[e];
               }
-              *reinterpret_cast<uint4*>(sP + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
+              *reinterpret_cast<uint4*>(sPb + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
                   make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                              pack_bf16x2(pv[6], pv[7]));
             }
@@ -654,7 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm2);
                 lr[e & 3] += pv[e];
               }
-              *reinterpret_cast<uint4*>(sP + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
+              *reinterpret_cast<uint4*>(sPb + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
                   make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                              pack_bf16x2(pv[6], pv[7]));
             }
@@ -667,6 +743,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           // far was 0) or, on a segment's first sub-tile, values that this
           // sub-tile's PV overwrites; either way nothing needs scaling.
           if (__any_sync(0xFFFFFFFFu, alpha != 1.f && alpha != 0.f)) {
+            // O must hold the previous sub-tile's PV before it is scaled.
+            mbar_wait(&bars[bPvDone + ((n_sub - 1) & 1)], ((n_sub - 1) >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+            tc_fence_after();
 #pragma unroll 1
             for (int j = 0; j < 8; ++j) {
               uint32_t o[16];
@@ -681,13 +760,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           //    block holds them (so its own wait covers the copy's reads).
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(&bars[bPMine]);  // the tensor core may start on this CTA's tokens
+          mbar_arrive(&bars[bPMine2 + pb]);  // the tensor core may start on this CTA's tokens
           named_bar_sync(pair_bar, 64);
           if (ch == static_cast<int>(c) && lane == 0) {
             // The peer's block for these rows is free: the peer's warps sent
             // this sub-tile's X from it after its previous PV had completed.
-            bulk_to_peer(peer_of(smem_u32(sP + c * 8192 + qd * 2048), peer), sP + c * 8192 + qd * 2048,
-                         kPQuadBytes, peer_of(smem_u32(&bars[bPIn]), peer));
+            bulk_to_peer(peer_of(smem_u32(sPb + c * 8192 + qd * 2048), peer), sPb + c * 8192 + qd * 2048,
+                         kPQuadBytes, peer_of(smem_u32(&bars[bPIn + pb]), peer));
             bulk_commit();
           }
         }
