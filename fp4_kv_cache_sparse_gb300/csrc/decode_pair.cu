@@ -44,7 +44,7 @@ constexpr int kPThreads = 448;
 constexpr int kHeads = 128;
 constexpr int kHalf = 256;
 constexpr int kStgSlots = 3;
-constexpr int kKvBufs = 3;
+constexpr int kKvBufs = 4;
 constexpr int kProdWarps = 4;
 constexpr int kSoftThreads = 256;
 constexpr int kLoaderWarp = 12;
@@ -56,7 +56,7 @@ constexpr uint32_t kPQuadBytes = 32 * 64;       // a quadrant's 32 heads x 32 to
 constexpr uint32_t kPInBytes = 4 * kPQuadBytes;  // the peer's quarter of P
 
 struct PairSmem {
-  static constexpr int kKV = 0;                  // 3 buffers x 4 chunks x [64 tokens x 128 B], SW128
+  static constexpr int kKV = 0;                  // 4 buffers x 4 chunks x [64 tokens x 128 B], SW128
   static constexpr int kP = kKV + kKvBufs * 32768;  // 2 buffers (sub-tile parity) x 2 chunks (32 tokens each)
                                                  // x [128 heads x 64 B] bf16, SW64; also the outgoing staging
                                                  // of the partial scores
@@ -75,14 +75,19 @@ struct PairSmem {
   static constexpr int kEnd = kScalar + 16;
   static constexpr int kAlloc = kEnd + 1024;
 };
+static_assert(PairSmem::kAlloc <= 227 * 1024, "dynamic shared memory of one CTA");
 
-enum PairBar {
-  bStgFull = 0, bStgFree = 3, bSclFull = 6, bSclFree = 8, bMaskFull = 10, bMaskFree = 12,
-  bKvFull = 14 /* [3 buffers] */, bKvFree = 17 /* [3] */, bQFull = 20, bSFull = 21 /* [2 S buffers] */,
-  bSUsed = 23 /* [2] */, bPMine2 = 25 /* [2] by sub-tile parity */, bPIn = 27 /* [2 P buffers] */,
-  bPvDone = 29 /* [2] */, bOReady = 31, bStatsIn = 32 /* [2] */, bDrain = 34,
-  bXFull = 35 /* [2 X buffers][8 warps] */, bMaxFull = 51 /* [4 quadrants] */
+// mbarrier indices; each range is as long as the count that indexes it.
+enum PairBar : int {
+  bStgFull = 0, bStgFree = bStgFull + kStgSlots, bSclFull = bStgFree + kStgSlots, bSclFree = bSclFull + 2,
+  bMaskFull = bSclFree + 2, bMaskFree = bMaskFull + 2, bKvFull = bMaskFree + 2, bKvFree = bKvFull + kKvBufs,
+  bQFull = bKvFree + kKvBufs, bSFull = bQFull + 1 /* [2 S buffers] */, bSUsed = bSFull + 2,
+  bPMine2 = bSUsed + 2 /* [2] by sub-tile parity */, bPIn = bPMine2 + 2 /* [2 P buffers] */, bPvDone = bPIn + 2,
+  bOReady = bPvDone + 2, bStatsIn = bOReady + 1 /* [2] */, bDrain = bStatsIn + 2,
+  bXFull = bDrain + 1 /* [2 X buffers][8 warps] */, bMaxFull = bXFull + 16 /* [4 quadrants] */,
+  kNumPairBars = bMaxFull + 4
 };
+static_assert(kNumPairBars <= 64, "the mbarrier area holds 64 barriers");
 
 // TMEM columns: S [0, 128) as two 64-column buffers, O [128, 384), Q [384, 512)
 // (this CTA's 256 dims of the query token as packed bf16 pairs: the A operand
@@ -318,6 +323,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         row[j] = valid ? id : -1;
         vbits[j] = __ballot_sync(0xFFFFFFFFu, valid);
       }
+      // The next tile's scales and the indices of the tile after it go out
+      // now, a whole tile of gathers ahead of their use.
+      load_scales(nxt, sc_nxt);
+      int32_t nxt2[4] = {-1, -1, -1, -1};
+      if (g + 2 < span.g_end) raw_ids(g + 2, nxt2);
       const uint32_t mp = n_tile & 1;
       if (n_tile >= 2) mbar_wait(&bars[bSclFree + mp], ((n_tile >> 1) - 1) & 1, abort_flag, p.d_error, kWaitNs);
 #pragma unroll
@@ -343,11 +353,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           tma_gather4(sStg + slot * 8192 + (lane & 7) * 1024, &kv_map, static_cast<int>(c) * kHalf, row[0], row[1],
                       row[2], row[3], &bars[bStgFull + slot]);
       }
-      // Next tile's scales and the indices of the tile after it, issued only
-      // now so that no load is in flight at this tile's arrivals.
-      load_scales(nxt, sc_nxt);
-      int32_t nxt2[4] = {-1, -1, -1, -1};
-      if (g + 2 < span.g_end) raw_ids(g + 2, nxt2);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         cur[j] = nxt[j];
@@ -359,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------------------
     // Dequantizers: staging slot (32 tokens x this CTA's 256 dims, raw e4m3)
     // + scales -> bf16 rows of a sub-tile buffer (two slots per 64-token
-    // sub-tile, three buffers in turn).  Lane L (0..127) handles items
+    // sub-tile, four buffers in turn).  Lane L (0..127) handles items
     // L + 128r (r = 0..3) of a slot; item i is token i >> 4, 16-dim segment
     // i & 15.
     // ------------------------------------------------------------------
@@ -434,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, 128, false, true);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, 256, false, true);
       const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
       const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
       uint32_t n_sub = 0, n_seg = 0;
@@ -452,19 +457,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         mma_commit(&bars[bSFull + sb]);
       };
       // O += P V over the 16-token K steps q0, q0+1 (this CTA's quarter or
-      // the peer's) of sub-tile buffer buf.
+      // the peer's) of sub-tile buffer buf: one N = 256 product per step, all
+      // four 64-dim chunks of this CTA's V at once, so P is read once.
       auto issue_pv = [&](uint32_t buf, uint32_t pb, int q0, bool init) {
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int ks = q0 + q;
-            const uint64_t a =
-                make_smem_desc(p_base + pb * 16384 + (ks >> 1) * 8192 + (ks & 1) * 32, 16, 512, kSwizzle64);
-            const uint64_t b =
-                make_smem_desc(kv_base + buf * 32768 + 2 * hh * 8192 + ks * 2048, 8192, 1024, kSwizzle128);
-            mma_bf16_ss(tO + 128 * hh, a, b, idesc_pv, !(init && q == 0));
-          }
+        for (int q = 0; q < 2; ++q) {
+          const int ks = q0 + q;
+          const uint64_t a =
+              make_smem_desc(p_base + pb * 16384 + (ks >> 1) * 8192 + (ks & 1) * 32, 16, 512, kSwizzle64);
+          const uint64_t b = make_smem_desc(kv_base + buf * 32768 + ks * 2048, 8192, 1024, kSwizzle128);
+          mma_bf16_ss(tO, a, b, idesc_pv, !(init && q == 0));
         }
       };
       for (int64_t g = span.g_begin; g < span.g_end;) {
