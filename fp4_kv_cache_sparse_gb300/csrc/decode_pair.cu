@@ -386,12 +386,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           mbar_wait(&bars[bStgFull + slot], suse & 1, abort_flag, p.d_error, kWaitNs);
           const uint8_t* stg = sStg + slot * 8192;
 #pragma unroll 1
-          for (int rb = 0; rb < 4; rb += 2) {
-            uint4 raw[2];
-            uint32_t sb[2];
+          for (int rb = 0; rb < 4; rb += 4) {
+            uint4 raw[4];
+            uint32_t sb[4];
             bool big = false;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
+            for (int r = 0; r < 4; ++r) {
               const int item = L + 128 * (rb + r);
               const int tt = item >> 4, s = item & 15;
               raw[r] = *reinterpret_cast<const uint4*>(stg + item * 16);
@@ -401,7 +401,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
             const bool any_big = __any_sync(0xFFFFFFFFu, big);
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
+            for (int r = 0; r < 4; ++r) {
               const int item = L + 128 * (rb + r);
               const int t = 32 * kk + (item >> 4), s = item & 15;  // row of the sub-tile
               uint32_t o[8];
