@@ -429,7 +429,7 @@ def main():
                      "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
                      "frac": frac, "traffic": traffic, "peak_source": pk["source"] + " (burst)",
                      "kernel": "decode kernel + split merge: CUDA events around the mla_sparse_decode call "
-                               "(the merge is ~4 % of it by the ncu launch list)"},
+                               "(the merge is ~5 % of it by the ncu launch list)"},
         "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 if dec_parts > 1 else 1) * args.steps,
