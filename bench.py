@@ -221,24 +221,49 @@ def time_kv_writer(dev, pk, steps, warmup, flush, tokens=1 << 20):
 
 
 def time_e2e(dw, dec, steps, warmup):
-    """Through the public API with HOST buffers: pinned q and indices copied
-    in, the decode, the output and LSE copied back, every step."""
+    """Through the public API with HOST buffers, as a serving loop runs it:
+    every step copies its q and indices in from pinned host memory, decodes,
+    and copies its output and LSE back.  Consecutive steps overlap: copies in
+    on one stream, the decode on the current stream, copies back on a third,
+    with two device buffer sets in turn (events order each set's reuse)."""
+    nb = 2
+    dev = dw.q.device
     q_h = dw.q.cpu().pin_memory()
     idx_h = dw.idx.cpu().pin_memory()
     xidx_h = dw.xidx.cpu().pin_memory() if dw.xidx is not None else None
-    out_h = torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(tuple(dw.q.shape[:3]), dtype=torch.float32).pin_memory()
-    q_d, idx_d = torch.empty_like(dw.q), torch.empty_like(dw.idx)
-    xidx_d = torch.empty_like(dw.xidx) if dw.xidx is not None else None
+    out_h = [torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    lse_h = [torch.empty(tuple(dw.q.shape[:3]), dtype=torch.float32).pin_memory() for _ in range(nb)]
+    q_d = [torch.empty_like(dw.q) for _ in range(nb)]
+    idx_d = [torch.empty_like(dw.idx) for _ in range(nb)]
+    xidx_d = [torch.empty_like(dw.xidx) if dw.xidx is not None else None for _ in range(nb)]
+    out_d = [torch.empty(tuple(dw.q.shape), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+    lse_d = [torch.empty(tuple(dw.q.shape[:3]), dtype=torch.float32, device=dev) for _ in range(nb)]
+    s_comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(nb)]
+    ev_dec = [torch.cuda.Event() for _ in range(nb)]
+    ev_out = [torch.cuda.Event() for _ in range(nb)]
+    count = [0]
 
     def step():
-        q_d.copy_(q_h, non_blocking=True)
-        idx_d.copy_(idx_h, non_blocking=True)
-        if xidx_d is not None:
-            xidx_d.copy_(xidx_h, non_blocking=True)
-        out, lse = dec(q_d, dw.kv, idx_d, dw.xkv, xidx_d)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        b = count[0] % nb
+        count[0] += 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_dec[b])  # the decode two steps back has read this input set
+            q_d[b].copy_(q_h, non_blocking=True)
+            idx_d[b].copy_(idx_h, non_blocking=True)
+            if xidx_h is not None:
+                xidx_d[b].copy_(xidx_h, non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        s_comp.wait_event(ev_out[b])  # this output set was read back two steps ago
+        dec(q_d[b], dw.kv, idx_d[b], dw.xkv, xidx_d[b], out=out_d[b], lse=lse_d[b])
+        ev_dec[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_dec[b])
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            lse_h[b].copy_(lse_d[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
     for _ in range(warmup):
         step()
@@ -249,7 +274,7 @@ def time_e2e(dw, dec, steps, warmup):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     h2d = q_h.numel() * 2 + idx_h.numel() * 4 + (xidx_h.numel() * 4 if xidx_h is not None else 0)
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    d2h = out_h[0].numel() * 2 + lse_h[0].numel() * 4
     return dt, h2d, d2h
 
 
