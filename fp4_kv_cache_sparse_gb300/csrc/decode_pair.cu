@@ -21,8 +21,9 @@
 // other its part of P, so both hold all of P for their O += P V.  P and the
 // received partial scores are double-buffered by sub-tile parity, so a
 // sub-tile's softmax does not wait for the previous sub-tile's PV; the bf16
-// tile is triple-buffered.  One thread issues each product as soon as its
-// inputs are ready.  Records reach shared memory by TMA row gathers
+// tile has four buffers, as a buffer is held from its dequantization to the
+// end of the PV that reads it.  One thread issues each product as soon as
+// its inputs are ready (O += P V as one 128x256x16 product per 16 tokens).  Records reach shared memory by TMA row gathers
 // (tile::gather4, 4 tokens per instruction, 256 bytes of a record per row)
 // into a 3-slot staging ring, so the dequantizing warps never have global
 // loads in flight when they publish a slot.
