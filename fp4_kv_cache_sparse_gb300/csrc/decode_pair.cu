@@ -59,10 +59,10 @@ constexpr uint32_t kPInBytes = 4 * kPQuadBytes;  // the peer's quarter of P
 struct PairSmem {
   static constexpr int kKV = 0;                  // 4 buffers x 4 chunks x [64 tokens x 128 B], SW128
   static constexpr int kP = kKV + kKvBufs * 32768;  // 2 buffers (sub-tile parity) x 2 chunks (32 tokens each)
-                                                 // x [128 heads x 64 B] bf16, SW64; also the outgoing staging
-                                                 // of the partial scores
+                                                 // x [128 heads x 64 B] bf16, SW64
   static constexpr int kX = kP + 2 * 16384;      // 2 buffers x 8 warps x [32 heads x 16 tokens] fp32 from the
-                                                 // peer, SW64 units
+                                                 // peer, SW64 units; a sub-tile's outgoing partial scores are
+                                                 // staged in the other parity's buffer
   static constexpr int kStg = kX + 2 * 16384;    // 3 slots x [32 tokens x 256 B] raw e4m3 (this CTA's dims)
   static constexpr int kScl = kStg + kStgSlots * 8192;  // 2 x [4][32] x 8 B e8m0 scales of this CTA's dims
                                                         // (token 4l + j of a 128-token tile at [j][l])
@@ -558,10 +558,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int i = 32 * qd + lane;  // head
     const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
     const uint32_t tS = tmem + lane_base + kColS, tO = tmem + lane_base + kColO, tQ = tmem + lane_base + kColQ;
-    // Staging block of this warp = rows 32 qd .. 32 qd + 31 of chunk ch of
-    // the sub-tile's P buffer; the quadrant's P rows of this CTA's chunk are
-    // the block of warp (qd, c).
-    const uint32_t stg_off = ch * 8192 + qd * 2048;
     const int pair_bar = 2 + qd;  // named barrier of the two warps of quadrant qd
     uint32_t n_tile = 0, n_sub = 0, n_seg = 0;
     float m = -INFINITY, l = 0.f;  // running max (shared by both CTAs) and this warp's part of the row sum
@@ -606,17 +602,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           const uint32_t tSb = tS + 64 * sb;
           uint8_t* sPb = sP + pb * 16384;
           const uint8_t* sXw = sX + pb * 16384 + warp * 2048;
+          // Outgoing staging: this warp's block of the other parity's X
+          // buffer.  The peer's partial scores of the next sub-tile land
+          // there only after this sub-tile's copy has reached the peer.
+          uint8_t* stg = sX + (pb ^ 1) * 16384 + warp * 2048;
           if (lane == 0) {
             mbar_expect_tx(&bars[bXFull + 8 * pb + warp], kXWarpBytes);
             if (ch == 0) mbar_expect_tx(&bars[bMaxFull + qd], 256);
           }
           mbar_wait(&bars[bSFull + sb], (n_sub >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          // The PV of two sub-tiles back is done: this P buffer (and this
-          // sub-tile's staging) is free, and the peer's P of that sub-tile
-          // has landed, so this P barrier is in its next phase.
-          if (n_sub >= 2) mbar_wait(&bars[bPvDone + pb], ((n_sub - 2) >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn + pb], kPInBytes);
-          // This warp's copies of the previous sub-tile out of its block are read.
+          // This warp's copies of earlier sub-tiles (out of this staging
+          // block two sub-tiles back, of P and of maxima) are read.
           if (lane == 0) bulk_wait_read();
           __syncwarp();
           tc_fence_after();
@@ -627,7 +623,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             tmem_ld16(tSb + 32 * peer + 16 * ch, v);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(sPb + stg_off + swz<64>(lane * 64 + u * 16)) =
+              *reinterpret_cast<uint4*>(stg + swz<64>(lane * 64 + u * 16)) =
                   make_uint4(__float_as_uint(__uint_as_float(v[4 * u]) * p.scale_log2),
                              __float_as_uint(__uint_as_float(v[4 * u + 1]) * p.scale_log2),
                              __float_as_uint(__uint_as_float(v[4 * u + 2]) * p.scale_log2),
@@ -636,11 +632,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            // The peer's X block of this warp and parity is free: this CTA
-            // has received the peer's P of two sub-tiles back (its PV,
-            // waited above, needed it), which the peer sent after its warps
-            // read that X.
-            bulk_to_peer(peer_of(smem_u32(sXw), peer), sPb + stg_off, kXWarpBytes,
+            // The peer's X block of this warp and parity is free: the
+            // peer's same warp read it (two sub-tiles back) before sending
+            // its tile maxima of the previous sub-tile, which this warp has
+            // received.
+            bulk_to_peer(peer_of(smem_u32(sXw), peer), stg, kXWarpBytes,
                          peer_of(smem_u32(&bars[bXFull + 8 * pb + warp]), peer));
             bulk_commit();
           }
@@ -654,10 +650,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             for (int e = 0; e < 4; ++e) mk |= ((mkw[e] >> shift) & 0xFu) << (4 * e);
           }
           mbar_wait(&bars[bXFull + 8 * pb + warp], (n_sub >> 1) & 1, abort_flag, p.d_error, kWaitNs);
-          // My P units sit in the staging block of warp (qd, c): both warps'
-          // staging copies must have been read.
-          if (lane == 0) bulk_wait_read();
-          named_bar_sync(pair_bar, 64);
+          // The PV of two sub-tiles back is done: this P buffer is free, and
+          // the peer's P of that sub-tile has landed, so this P barrier is
+          // in its next phase.  (The quadrant's P copy of that sub-tile was
+          // read before the pair barriers of the sub-tile between.)
+          if (n_sub >= 2) mbar_wait(&bars[bPvDone + pb], ((n_sub - 2) >> 1) & 1, abort_flag, p.d_error, kWaitNs);
+          if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bPIn + pb], kPInBytes);
           const float mm = m == -INFINITY ? 0.f : m;  // all y are -inf when m is
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -759,15 +757,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
             tmem_wait_st();
           }
-          // 4. The quadrant's P rows to the peer, from the warp whose staging
-          //    block holds them (so its own wait covers the copy's reads).
+          // 4. The quadrant's P rows to the peer, copied by warp (qd, c),
+          //    whose wait at the start of the next sub-tile covers the
+          //    copy's reads.
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&bars[bPMine2 + pb]);  // the tensor core may start on this CTA's tokens
           named_bar_sync(pair_bar, 64);
           if (ch == static_cast<int>(c) && lane == 0) {
-            // The peer's block for these rows is free: the peer's warps sent
-            // this sub-tile's X from it after its previous PV had completed.
+            // The peer's block for these rows is free: the peer's warps
+            // waited for their PV of two sub-tiles back (its last reader)
+            // before the score pass that preceded the maxima received above.
             bulk_to_peer(peer_of(smem_u32(sPb + c * 8192 + qd * 2048), peer), sPb + c * 8192 + qd * 2048,
                          kPQuadBytes, peer_of(smem_u32(&bars[bPIn + pb]), peer));
             bulk_commit();
