@@ -53,13 +53,14 @@ constexpr int kIssueWarp = 13;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLazy = 8.0f;
 constexpr uint32_t kXWarpBytes = 32 * 64;       // one softmax warp's 32 heads x 16 tokens of fp32 scores
-constexpr uint32_t kPQuadBytes = 32 * 64;       // a quadrant's 32 heads x 32 tokens of bf16 P
-constexpr uint32_t kPInBytes = 4 * kPQuadBytes;  // the peer's quarter of P
+constexpr uint32_t kPWarpBytes = 32 * 32;       // one softmax warp's 32 heads x 16 tokens of bf16 P
+constexpr uint32_t kPInBytes = 8 * kPWarpBytes;  // the peer's quarter of P
 
 struct PairSmem {
   static constexpr int kKV = 0;                  // 4 buffers x 4 chunks x [64 tokens x 128 B], SW128
-  static constexpr int kP = kKV + kKvBufs * 32768;  // 2 buffers (sub-tile parity) x 2 chunks (32 tokens each)
-                                                 // x [128 heads x 64 B] bf16, SW64
+  static constexpr int kP = kKV + kKvBufs * 32768;  // 2 buffers (sub-tile parity) x 4 chunks (16 tokens each:
+                                                 // K steps of O += P V) x [128 heads x 32 B] bf16, SW32, so
+                                                 // each softmax warp's P rows are one contiguous 1 KB block
   static constexpr int kX = kP + 2 * 16384;      // 2 buffers x 8 warps x [32 heads x 16 tokens] fp32 from the
                                                  // peer, SW64 units; a sub-tile's outgoing partial scores are
                                                  // staged in the other parity's buffer
@@ -465,7 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         for (int q = 0; q < 2; ++q) {
           const int ks = q0 + q;
           const uint64_t a =
-              make_smem_desc(p_base + pb * 16384 + (ks >> 1) * 8192 + (ks & 1) * 32, 16, 512, kSwizzle64);
+              make_smem_desc(p_base + pb * 16384 + ks * 4096, 16, 256, kSwizzle32);
           const uint64_t b = make_smem_desc(kv_base + buf * 32768 + ks * 2048, 8192, 1024, kSwizzle128);
           mma_bf16_ss(tO, a, b, idesc_pv, !(init && q == 0));
         }
@@ -602,6 +603,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           const uint32_t tSb = tS + 64 * sb;
           uint8_t* sPb = sP + pb * 16384;
           const uint8_t* sXw = sX + pb * 16384 + warp * 2048;
+          // This warp's P rows: chunk 2c + ch (its 16 tokens) of the P buffer.
+          uint8_t* sPw = sPb + (2 * static_cast<int>(c) + ch) * 4096;
           // Outgoing staging: this warp's block of the other parity's X
           // buffer.  The peer's partial scores of the next sub-tile land
           // there only after this sub-tile's copy has reached the peer.
@@ -683,7 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm);
                 ls[e & 3] += pv[e];
               }
-              *reinterpret_cast<uint4*>(sPb + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
+              *reinterpret_cast<uint4*>(sPw + swz<32>(i * 32 + w * 16)) =
                   make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                              pack_bf16x2(pv[6], pv[7]));
             }
@@ -731,7 +734,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 pv[e] = ex2_approx(__uint_as_float(v[8 * w + e]) - mm2);
                 lr[e & 3] += pv[e];
               }
-              *reinterpret_cast<uint4*>(sPb + c * 8192 + swz<64>(i * 64 + (2 * ch + w) * 16)) =
+              *reinterpret_cast<uint4*>(sPw + swz<32>(i * 32 + w * 16)) =
                   make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
                              pack_bf16x2(pv[6], pv[7]));
             }
@@ -757,19 +760,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
             }
             tmem_wait_st();
           }
-          // 4. The quadrant's P rows to the peer, copied by warp (qd, c),
-          //    whose wait at the start of the next sub-tile covers the
-          //    copy's reads.
+          // 4. My P rows (1 KB) to the peer; this warp's wait at the start
+          //    of the next sub-tile covers the copy's reads.
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&bars[bPMine2 + pb]);  // the tensor core may start on this CTA's tokens
-          named_bar_sync(pair_bar, 64);
-          if (ch == static_cast<int>(c) && lane == 0) {
+          __syncwarp();
+          if (lane == 0) {
             // The peer's block for these rows is free: the peer's warps
             // waited for their PV of two sub-tiles back (its last reader)
             // before the score pass that preceded the maxima received above.
-            bulk_to_peer(peer_of(smem_u32(sPb + c * 8192 + qd * 2048), peer), sPb + c * 8192 + qd * 2048,
-                         kPQuadBytes, peer_of(smem_u32(&bars[bPIn + pb]), peer));
+            uint8_t* blk = sPw + qd * 1024;
+            bulk_to_peer(peer_of(smem_u32(blk), peer), blk, kPWarpBytes, peer_of(smem_u32(&bars[bPIn + pb]), peer));
             bulk_commit();
           }
         }
