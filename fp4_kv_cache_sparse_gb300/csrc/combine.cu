@@ -19,6 +19,10 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const int32_t* __r
                                                              const float* __restrict__ lse_part,
                                                              uint16_t* __restrict__ out, float* __restrict__ lse,
                                                              int nq, int h_q, int skip_single) {
+  // Launched as a programmatic dependent of the decode kernel: wait until
+  // that grid has completed and its partials are visible (returns at once
+  // for an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= static_cast<int64_t>(nq) * h_q) return;
@@ -73,9 +77,21 @@ cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, con
   const int64_t rows = static_cast<int64_t>(nq) * h_q;
   const int64_t blocks = (rows + kWarps - 1) / kWarps;
   if (blocks == 0) return cudaSuccess;
-  combine_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(d_num_splits, o_part, lse_part, out, lse,
-                                                                            nq, h_q, skip_single ? 1 : 0);
-  return cudaGetLastError();
+  // Programmatic stream serialization: the merge's blocks may be scheduled
+  // while the preceding kernel drains; each waits for it (griddepcontrol)
+  // before reading anything.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, d_num_splits, o_part, lse_part, out, lse, nq, h_q,
+                            skip_single ? 1 : 0);
 }
 
 }  // namespace mla
