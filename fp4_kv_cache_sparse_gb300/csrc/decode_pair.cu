@@ -552,8 +552,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // sends its 16 columns of the peer's quarter of the partial scores to the
     // peer's same warp and receives the peer's for its columns of this
     // quarter; per-head tile maxima of both warps of a quadrant are swapped
-    // with the peer so both CTAs keep identical running maxima; each
-    // quadrant's P rows travel to the peer, so both hold all of P for PV.
+    // with the peer so both CTAs keep identical running maxima; each warp's
+    // P (its 32 heads x 16 tokens) travels to the peer, so both hold all of
+    // P for PV.
     // ------------------------------------------------------------------
     const int qd = warp & 3, ch = warp >> 2;
     const int i = 32 * qd + lane;  // head
