@@ -282,6 +282,7 @@ def time_metadata(problem, dev, n=20, warmup=3):
     """mla_get_metadata through the public API (once per decode loop, so
     timed apart from the step): host wall time per call, including its
     kernel, synchronized."""
+    import fp4_kv_cache_sparse_gb300 as mla
     for _ in range(warmup):
         mla.get_metadata(problem, 0, dev)
     torch.cuda.synchronize()
