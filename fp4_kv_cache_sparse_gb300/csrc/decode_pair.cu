@@ -563,34 +563,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int pair_bar = 2 + qd;  // named barrier of the two warps of quadrant qd
     uint32_t n_tile = 0, n_sub = 0, n_seg = 0;
     float m = -INFINITY, l = 0.f;  // running max (shared by both CTAs) and this warp's part of the row sum
+    // Q row i of query token qx, dims [128 ch, 128 ch + 128) of my half, into
+    // TMEM as packed bf16 pairs (columns 64 ch .. 64 ch + 63 of the Q area).
+    auto q_src = [&](int qx) {
+      return reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qx) * kHeads + i) * kD +
+                                            static_cast<int>(c) * kHalf + ch * 128);
+    };
+    auto load_q = [&](int qx) {
+      const uint4* src = q_src(qx);
+#pragma unroll 1
+      for (int j = 0; j < 2; ++j) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 w = __ldg(src + j * 8 + u);
+          v[4 * u] = w.x;
+          v[4 * u + 1] = w.y;
+          v[4 * u + 2] = w.z;
+          v[4 * u + 3] = w.w;
+        }
+        tmem_st32(tQ + 64 * ch + 32 * j, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[bQFull]);
+    };
+    if (span.g_begin < span.g_end) load_q(static_cast<int>(span.g_begin / p.T));
     for (int64_t g = span.g_begin; g < span.g_end;) {
       const int qidx = static_cast<int>(g / p.T);
       const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
       const int64_t seg_begin = g;
       if (warp == 0 && lane == 0) mbar_expect_tx(&bars[bStatsIn + (n_seg & 1)], 1024);
-      {
-        // Q row i, dims [128 ch, 128 ch + 128) of my half, into TMEM as
-        // packed bf16 pairs (columns 64 ch .. 64 ch + 63 of the Q area).
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qidx) * kHeads + i) * kD +
-                                                          static_cast<int>(c) * kHalf + ch * 128);
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          uint32_t v[32];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 w = __ldg(src + j * 8 + u);
-            v[4 * u] = w.x;
-            v[4 * u + 1] = w.y;
-            v[4 * u + 2] = w.z;
-            v[4 * u + 3] = w.w;
-          }
-          tmem_st32(tQ + 64 * ch + 32 * j, v);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars[bQFull]);
-      }
       for (; g < seg_end; ++g, ++n_tile) {
+        if (g + 1 == seg_end && seg_end < span.g_end) {
+          // The next query token's Q rows into L2 now, two sub-tiles before
+          // they are loaded.
+          const uint4* nq = q_src(qidx + 1);
+          asm volatile("prefetch.L2 [%0];" ::"l"(nq));
+          asm volatile("prefetch.L2 [%0];" ::"l"(nq + 8));
+        }
         // Validity of the 128-token tile: bit b of word e covers token 4b + e.
         const uint32_t mp = n_tile & 1;
         mbar_wait(&bars[bMaskFull + mp], (n_tile >> 1) & 1, abort_flag, p.d_error, kWaitNs);
@@ -778,6 +789,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
       }
 
+      // The next query token's Q goes into TMEM first (this token's last
+      // S = Q K^T has completed: its sub-tile's softmax waited for it), so
+      // that the next S runs during this epilogue; O is safe until this
+      // warp's next P lets the tensor core start the next O += P V.
+      if (seg_end < span.g_end) load_q(qidx + 1);
       // Epilogue of this query token (or split): the row sum over both
       // column halves of both CTAs, added in CTA order so both CTAs agree
       // bit for bit; then my O columns / l.
