@@ -800,6 +800,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const uint32_t sp = n_seg & 1;
       sStatsOut[128 * ch + i] = l;
       fence_proxy_async_smem();
+      // Every warp's copies out of the P buffers have been read once all
+      // pass this barrier: the O rows below are staged there.
+      if (lane == 0) bulk_wait_read();
       named_bar_sync(1, kSoftThreads);
       if (warp == 0 && lane == 0) {
         bulk_to_peer(peer_of(smem_u32(sStats + sp * 256), peer), sStatsOut, 1024,
@@ -830,28 +833,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_wait(&bars[bOReady], n_seg & 1, abort_flag, p.d_error, kWaitNs);
       __syncwarp();
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(qidx) * p.h_q + i;
+      // O rows leave through this warp's 4 KB of the P buffers (idle now:
+      // every PV of this token is done, and the peer sends its next P only
+      // after this CTA's next partial scores), so that the global stores go
+      // out as whole row pieces: 4 lanes x 16 B of one bf16 row, or
+      // 8 lanes x 16 B of one fp32 row, per store.
+      uint8_t* ost = sP + warp * 4096;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t o[32];
         tmem_ld32(tO + 128 * ch + 32 * j, o);
         const int d0 = static_cast<int>(c) * kHalf + 128 * ch + 32 * j;
         if (direct) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + row * kD + d0);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * u + 0]) * linv, __uint_as_float(o[8 * u + 1]) * linv),
-                                pack_bf16x2(__uint_as_float(o[8 * u + 2]) * linv, __uint_as_float(o[8 * u + 3]) * linv),
-                                pack_bf16x2(__uint_as_float(o[8 * u + 4]) * linv, __uint_as_float(o[8 * u + 5]) * linv),
-                                pack_bf16x2(__uint_as_float(o[8 * u + 6]) * linv, __uint_as_float(o[8 * u + 7]) * linv));
+            *reinterpret_cast<uint4*>(ost + swz<64>(lane * 64 + u * 16)) =
+                make_uint4(pack_bf16x2(__uint_as_float(o[8 * u + 0]) * linv, __uint_as_float(o[8 * u + 1]) * linv),
+                           pack_bf16x2(__uint_as_float(o[8 * u + 2]) * linv, __uint_as_float(o[8 * u + 3]) * linv),
+                           pack_bf16x2(__uint_as_float(o[8 * u + 4]) * linv, __uint_as_float(o[8 * u + 5]) * linv),
+                           pack_bf16x2(__uint_as_float(o[8 * u + 6]) * linv, __uint_as_float(o[8 * u + 7]) * linv));
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = 8 * k + (lane >> 2), u = lane & 3;  // row of this warp, 16-byte piece
+            const uint4 v = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + u * 16));
+            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(qidx) * p.h_q + 32 * qd + r) * kD + d0 + 8 * u) = v;
+          }
         } else if (split_ok) {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + (split * p.h_q + i) * kD + d0);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            dst[u] = make_float4(__uint_as_float(o[4 * u + 0]) * linv, __uint_as_float(o[4 * u + 1]) * linv,
-                                 __uint_as_float(o[4 * u + 2]) * linv, __uint_as_float(o[4 * u + 3]) * linv);
+            *reinterpret_cast<float4*>(ost + swz<128>(lane * 128 + u * 16)) =
+                make_float4(__uint_as_float(o[4 * u + 0]) * linv, __uint_as_float(o[4 * u + 1]) * linv,
+                            __uint_as_float(o[4 * u + 2]) * linv, __uint_as_float(o[4 * u + 3]) * linv);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int r = 4 * k + (lane >> 3), u = lane & 7;
+            const float4 v = *reinterpret_cast<const float4*>(ost + swz<128>(r * 128 + u * 16));
+            *reinterpret_cast<float4*>(p.ws_o + (split * p.h_q + 32 * qd + r) * kD + d0 + 4 * u) = v;
+          }
         }
+        __syncwarp();  // this warp's staging block is rewritten next
       }
+      // No warp sends the next partial scores (after which the peer's next P
+      // lands here) or writes the next P before every warp's O rows have
+      // been read out of the P buffers.
+      named_bar_sync(1, kSoftThreads);
       tc_fence_before();
       ++n_seg;
     }
