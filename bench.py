@@ -316,6 +316,29 @@ def oracle_rate(w, budget_s=12.0, max_queries=None):
     return done_flops / done_s / 1e12, desc, done_s, oracle.num_threads()
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x: a job's step time is its slowest
+    rank's.  Works on any initialized backend (NCCL on GPUs, gloo on CPU)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(wid: int, rank: int) -> int:
+    """Each rank decodes its own replica of the workload, drawn from its own
+    seed (weak scaling: per-rank work is fixed as ranks are added)."""
+    return synth.SEED_BASE + wid + 7919 * rank
+
+
+def job_rate(world: int, per_rank_units: float, step_s: float, scale: float = 1e12) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return world * per_rank_units / step_s / scale
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -399,25 +422,16 @@ def main():
 
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
     wid = int(args.workload) if args.workload.isdigit() else synth.BY_NAME[args.workload].id
-    w = synth.make_workload(wid, seed=synth.SEED_BASE + wid + 7919 * rank, batch=args.batch, pool=args.pool)
+    w = synth.make_workload(wid, seed=replica_seed(wid, rank), batch=args.batch, pool=args.pool)
     flops, kvb = synth.flops(w), synth.kv_bytes(w)
     dw, dec = build_device(w, dev)
     dec_parts = dec.num_parts
     ms, t0, t1 = time_decode(dw, dec, args.steps, args.warmup, flush, barrier)
-    step_s = statistics.mean(ms) * 1e-3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_s = float(t.item())
-    value = world * flops / step_s / 1e12
+    step_s = max_over_ranks(statistics.mean(ms) * 1e-3, world, dev)
+    value = job_rate(world, flops, step_s)
     e2e_s, h2d, d2h = (float("nan"), 0, 0) if args.no_e2e else time_e2e(dw, dec, max(20, args.steps // 20),
                                                                           args.warmup)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
     # The dominant kernel is the decode.  The split merge is launched inside
     # the same call and cannot be timed apart with events from outside it, so
     # the achieved figure uses the whole call: it understates the decode
@@ -434,7 +448,7 @@ def main():
         torch.cuda.empty_cache()
         kv_writer = time_kv_writer(dev, pk, max(20, args.steps // 50), args.warmup, flush)
         for cid in SECONDARY:
-            wc = synth.make_workload(cid, seed=synth.SEED_BASE + cid + 7919 * rank)
+            wc = synth.make_workload(cid, seed=replica_seed(cid, rank))
             f2, b2 = synth.flops(wc), synth.kv_bytes(wc)
             dwc, decc = build_device(wc, dev)
             msc, _, _ = time_decode(dwc, decc, max(50, args.steps // 10), args.warmup, flush, barrier)
@@ -464,7 +478,7 @@ def main():
                    "h_q": w.cfg.h_q, "head_dim": 512, "topk": w.cfg.topk, "pool_per_seq": w.cfg.pool,
                    "kv_format": "fp8_528", "l2": "flushed between steps (512 MB write, outside the timed events)",
                    "step": "mla_sparse_decode: decode kernel + split merge", "parallelism": f"replicas x{world}"},
-        "kv_gbs": world * kvb / step_s / 1e9,
+        "kv_gbs": job_rate(world, kvb, step_s, 1e9),
         "roofline": {"bound": bound, "achieved": per_rank_achieved,
                      "peak": pk["bf16_tflops"] if bound == "tensor" else pk["hbm_gbs"],
                      "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
@@ -473,7 +487,7 @@ def main():
                      "frac_fp8_peak": (per_rank_achieved / (2 * pk["bf16_tflops"])) if bound == "tensor" else None,
                      "kernel": "decode kernel + split merge: CUDA events around the mla_sparse_decode call "
                                "(the merge is ~5 % of it by the ncu launch list)"},
-        "e2e": {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_rate(world, flops, e2e_s), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 if dec_parts > 1 else 1) * args.steps,
         "metadata_us": round(metadata_us, 1),
