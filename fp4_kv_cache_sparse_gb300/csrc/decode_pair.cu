@@ -123,6 +123,13 @@ __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// 32 bytes from global memory (read-only path); p must be 32-byte aligned.
+__device__ __forceinline__ void ldg_v8(const void* p, uint32_t* r) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
 // Non-blocking test of a phase's completion.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -569,18 +576,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       return reinterpret_cast<const uint4*>(p.q + (static_cast<int64_t>(qx) * kHeads + i) * kD +
                                             static_cast<int>(c) * kHalf + ch * 128);
     };
+    // Each lane's rows start on 256-byte boundaries of q, so with q 32-byte
+    // aligned the row goes in 32-byte loads (half the requests of 16-byte
+    // ones); otherwise in 16-byte loads.
+    const bool q_al32 = (reinterpret_cast<uintptr_t>(p.q) & 31) == 0;
     auto load_q = [&](int qx) {
       const uint4* src = q_src(qx);
 #pragma unroll 1
       for (int j = 0; j < 2; ++j) {
         uint32_t v[32];
+        if (q_al32) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 w = __ldg(src + j * 8 + u);
-          v[4 * u] = w.x;
-          v[4 * u + 1] = w.y;
-          v[4 * u + 2] = w.z;
-          v[4 * u + 3] = w.w;
+          for (int u = 0; u < 4; ++u) ldg_v8(src + j * 8 + 2 * u, v + 8 * u);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 w = __ldg(src + j * 8 + u);
+            v[4 * u] = w.x;
+            v[4 * u + 1] = w.y;
+            v[4 * u + 2] = w.z;
+            v[4 * u + 3] = w.w;
+          }
         }
         tmem_st32(tQ + 64 * ch + 32 * j, v);
       }

@@ -205,3 +205,24 @@ def test_topk1_returns_the_latent():
         got = out[b, 0].view(torch.int16).cpu().numpy().view(np.uint16)
         assert np.all(got == k[None, :])
     compare(out, lse, w, all_queries(w))
+
+
+def test_q_alignment_paths_agree():
+    """q only 16-byte aligned (the contract's minimum) takes the kernel's
+    16-byte load path; 32-byte aligned q the 32-byte one: both give the same
+    bits, and both match the oracle."""
+    w = synth.make_workload(2, batch=1, workers=1)
+    dw = DeviceWorkload(w)
+    out_a, lse_a, err_a = dw.run()
+    assert int(dw.q.data_ptr()) % 32 == 0
+    n = dw.q.numel()
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device=dw.dev)
+    q16 = buf[8:].view(dw.q.shape)  # 16 bytes past a 32-byte boundary
+    assert int(q16.data_ptr()) % 32 == 16
+    q16.copy_(dw.q)
+    dw.q = q16
+    out_b, lse_b, err_b = dw.run()
+    assert err_a == 0 and err_b == 0
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(lse_a, lse_b)
+    compare(out_b, lse_b, w, all_queries(w))
