@@ -130,6 +130,13 @@ __device__ __forceinline__ void ldg_v8(const void* p, uint32_t* r) {
                : "l"(p));
 }
 
+// 32 bytes to global memory; p must be 32-byte aligned.
+__device__ __forceinline__ void stg_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 // Non-blocking test of a phase's completion.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -580,6 +587,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // aligned the row goes in 32-byte loads (half the requests of 16-byte
     // ones); otherwise in 16-byte loads.
     const bool q_al32 = (reinterpret_cast<uintptr_t>(p.q) & 31) == 0;
+    // Likewise the O rows out: 32-byte stores when the destination allows.
+    const bool out_al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
+    const bool ws_al32 = (reinterpret_cast<uintptr_t>(p.ws_o) & 31) == 0;
     auto load_q = [&](int qx) {
       const uint4* src = q_src(qx);
 #pragma unroll 1
@@ -852,8 +862,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       // O rows leave through this warp's 4 KB of the P buffers (idle now:
       // every PV of this token is done, and the peer sends its next P only
       // after this CTA's next partial scores), so that the global stores go
-      // out as whole row pieces: 4 lanes x 16 B of one bf16 row, or
-      // 8 lanes x 16 B of one fp32 row, per store.
+      // out as whole row pieces: 64 bytes of one bf16 row or 128 bytes of
+      // one fp32 row per group of lanes (32 bytes per lane when aligned).
       uint8_t* ost = sP + warp * 4096;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
@@ -869,11 +879,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                            pack_bf16x2(__uint_as_float(o[8 * u + 4]) * linv, __uint_as_float(o[8 * u + 5]) * linv),
                            pack_bf16x2(__uint_as_float(o[8 * u + 6]) * linv, __uint_as_float(o[8 * u + 7]) * linv));
           __syncwarp();
+          if (out_al32) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = 8 * k + (lane >> 2), u = lane & 3;  // row of this warp, 16-byte piece
-            const uint4 v = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + u * 16));
-            *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(qidx) * p.h_q + 32 * qd + r) * kD + d0 + 8 * u) = v;
+            for (int k = 0; k < 2; ++k) {
+              const int r = 16 * k + (lane >> 1), h = lane & 1;  // row of this warp, 32-byte piece
+              const uint4 a = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + (2 * h) * 16));
+              const uint4 b = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + (2 * h + 1) * 16));
+              stg_v8(p.out + (static_cast<int64_t>(qidx) * p.h_q + 32 * qd + r) * kD + d0 + 16 * h, a, b);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = 8 * k + (lane >> 2), u = lane & 3;  // row of this warp, 16-byte piece
+              const uint4 v = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + u * 16));
+              *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(qidx) * p.h_q + 32 * qd + r) * kD + d0 + 8 * u) =
+                  v;
+            }
           }
         } else if (split_ok) {
 #pragma unroll
@@ -882,11 +903,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
                 make_float4(__uint_as_float(o[4 * u + 0]) * linv, __uint_as_float(o[4 * u + 1]) * linv,
                             __uint_as_float(o[4 * u + 2]) * linv, __uint_as_float(o[4 * u + 3]) * linv);
           __syncwarp();
+          if (ws_al32) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int r = 4 * k + (lane >> 3), u = lane & 7;
-            const float4 v = *reinterpret_cast<const float4*>(ost + swz<128>(r * 128 + u * 16));
-            *reinterpret_cast<float4*>(p.ws_o + (split * p.h_q + 32 * qd + r) * kD + d0 + 4 * u) = v;
+            for (int k = 0; k < 4; ++k) {
+              const int r = 8 * k + (lane >> 2), h = lane & 3;
+              const uint4 a = *reinterpret_cast<const uint4*>(ost + swz<128>(r * 128 + (2 * h) * 16));
+              const uint4 b = *reinterpret_cast<const uint4*>(ost + swz<128>(r * 128 + (2 * h + 1) * 16));
+              stg_v8(p.ws_o + (split * p.h_q + 32 * qd + r) * kD + d0 + 8 * h, a, b);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int r = 4 * k + (lane >> 3), u = lane & 7;
+              const float4 v = *reinterpret_cast<const float4*>(ost + swz<128>(r * 128 + u * 16));
+              *reinterpret_cast<float4*>(p.ws_o + (split * p.h_q + 32 * qd + r) * kD + d0 + 4 * u) = v;
+            }
           }
         }
         __syncwarp();  // this warp's staging block is rewritten next

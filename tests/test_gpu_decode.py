@@ -207,21 +207,38 @@ def test_topk1_returns_the_latent():
     compare(out, lse, w, all_queries(w))
 
 
-def test_q_alignment_paths_agree():
-    """q only 16-byte aligned (the contract's minimum) takes the kernel's
-    16-byte load path; 32-byte aligned q the 32-byte one: both give the same
-    bits, and both match the oracle."""
+def _off16(shape, dtype, dev):
+    """A contiguous tensor starting 16 bytes past a 32-byte boundary."""
+    n = math.prod(shape)
+    pad = 16 // torch.empty((), dtype=dtype).element_size()
+    t = torch.empty(n + pad, dtype=dtype, device=dev)[pad:].view(shape)
+    assert int(t.data_ptr()) % 32 == 16
+    return t
+
+
+def test_alignment_paths_agree():
+    """q, out and the workspace only 16-byte aligned (the contract's minimum)
+    take the kernel's 16-byte load and store paths; 32-byte aligned buffers
+    the 32-byte ones: both give the same bits, and both match the oracle
+    (one query token's tiles are split over many parts, so the workspace
+    path runs too)."""
     w = synth.make_workload(2, batch=1, workers=1)
     dw = DeviceWorkload(w)
-    out_a, lse_a, err_a = dw.run()
-    assert int(dw.q.data_ptr()) % 32 == 0
-    n = dw.q.numel()
-    buf = torch.empty(n + 8, dtype=torch.bfloat16, device=dw.dev)
-    q16 = buf[8:].view(dw.q.shape)  # 16 bytes past a 32-byte boundary
-    assert int(q16.data_ptr()) % 32 == 16
+    dec = dw.decoder()
+    out_a, lse_a, err_a = dw.run(dec=dec)
+    assert int(dw.q.data_ptr()) % 32 == 0 and int(out_a.data_ptr()) % 32 == 0
+    assert int(dec.workspace.data_ptr()) % 32 == 0
+    assert dec.num_parts > 1
+    q16 = _off16(tuple(dw.q.shape), torch.bfloat16, dw.dev)
     q16.copy_(dw.q)
     dw.q = q16
-    out_b, lse_b, err_b = dw.run()
+    dec.workspace = _off16((dec.workspace.numel(),), torch.uint8, dw.dev)
+    out16 = _off16(tuple(out_a.shape), torch.bfloat16, dw.dev)
+    dec.error.zero_()
+    out_b, lse_b = dec(dw.q, dw.kv, dw.idx, out=out16)
+    torch.cuda.synchronize()
+    err_b = int(dec.error.item())
+    assert out_b.data_ptr() == out16.data_ptr()
     assert err_a == 0 and err_b == 0
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
     assert torch.equal(lse_a, lse_b)
