@@ -706,38 +706,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    tried = true;
-  }
-  return fn;
-}
 
 }  // namespace
 
 template <int NH>
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
   constexpr int smem = Smem<NH>::kAlloc;
-  static bool configured = false;  // benign race: the attribute call is idempotent
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e0 = max_dynamic_smem_once(configured, reinterpret_cast<const void*>(sparse_decode_kernel<NH>), smem);
+  if (e0 != cudaSuccess) return e0;
   // Q viewed as [nq * h_q rows][512 bf16]; a box is NH rows x 64 dims, 128-byte swizzled.
-  EncodeTiledFn enc = encode_tiled();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap q_map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.nq) * p.h_q};

@@ -941,24 +941,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    tried = true;
-  }
-  return fn;
-}
 
 }  // namespace
 
@@ -966,13 +948,10 @@ int decode_pair_smem_bytes() { return PairSmem::kAlloc; }
 
 cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_t stream) {
   constexpr int smem = PairSmem::kAlloc;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  EncodeTiledFn enc = encode_tiled_fn();
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e0 = max_dynamic_smem_once(configured, reinterpret_cast<const void*>(sparse_decode_pair_kernel), smem);
+  if (e0 != cudaSuccess) return e0;
+  EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   CUtensorMap kv_map;
   {

@@ -2,8 +2,10 @@
 // kernels of the library (not installed, not part of the ABI).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mla {
@@ -57,5 +59,36 @@ cudaError_t launch_dequant(int kv_format, const uint8_t* records, int64_t n, uin
 
 cudaError_t launch_kv_write(int kv_format, const uint16_t* latents, const int32_t* slots, int64_t n, uint8_t* pool,
                             int64_t pool_tokens, int32_t* d_error, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled from the driver, looked up once (thread-safe
+// static initialization); nullptr if the driver does not offer it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline EncodeTiledFn tensor_map_encoder() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    const bool ok = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                        cudaSuccess &&
+                    q == cudaDriverEntryPointSuccess;
+    return ok ? reinterpret_cast<EncodeTiledFn>(f) : EncodeTiledFn{nullptr};
+  }();
+  return fn;
+}
+
+// A kernel's dynamic shared memory limit, set once per device: the attribute
+// belongs to the current device's context, so bit d of `done` records device
+// d (devices past 63 set it on every call).
+inline cudaError_t max_dynamic_smem_once(std::atomic<uint64_t>& done, const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 }  // namespace mla
