@@ -172,11 +172,12 @@ def test_growing_scores_move_the_max_every_tile(h_q):
 
 
 @pytest.mark.parametrize("cid", [1, 2])
-@pytest.mark.parametrize("num_sms", [1, 3, 152, 100000])
+@pytest.mark.parametrize("num_sms", [1, 3, 20, 152, 100000])
 def test_split_counts_do_not_change_results(num_sms, cid):
     """From one part (no split) to one tile per part (every query split into
-    all its tiles); 64 heads (merged by the combine kernel) and 128 heads
-    (merged inside the decode kernel by the last split to finish)."""
+    all its tiles); 64 heads and 128 heads, merged by the combine kernel.
+    20 SMs give parts of 10 tiles over 16-tile query tokens, so some parts
+    end one token's split and start the next's."""
     w = synth.make_workload(cid, batch=3, workers=1)
     dw = DeviceWorkload(w)
     out, lse, err = dw.run(num_sms=num_sms)
