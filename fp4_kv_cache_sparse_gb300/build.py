@@ -59,6 +59,16 @@ def _check_spills(src: str, log: str) -> list[str]:
     return bad
 
 
+def refuse_spills(sources: list[str], logs: list[str]) -> None:
+    """Raise SpillError naming every kernel whose ptxas report shows spill
+    stores or loads (the library is then not linked)."""
+    spills = []
+    for src, log in zip(sources, logs):
+        spills += _check_spills(src, log)
+    if spills:
+        raise SpillError("register spills (the build refuses them):\n" + "\n".join(spills))
+
+
 def _compile(src: str) -> tuple[str, str]:
     obj = os.path.join(BUILD, src.replace(".cu", ".o"))
     cmd = [nvcc(), *ARCH, *FLAGS, "-I", os.path.join(HERE, "..", "include"), "-c",
@@ -75,17 +85,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
         results = list(ex.map(_compile, SOURCES))
-    spills = []
-    report = []
-    for src, (obj, log) in zip(SOURCES, results):
-        spills += _check_spills(src, log)
-        report.append(log)
+    report = [log for _, log in results]
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write("\n".join(report))
     if verbose:
         print("\n".join(report))
-    if spills:
-        raise SpillError("register spills (the build refuses them):\n" + "\n".join(spills))
+    refuse_spills(SOURCES, report)
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)

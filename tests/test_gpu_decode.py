@@ -91,13 +91,25 @@ def test_heads_and_ragged_topk(h_q, topk):
     compare(out, lse, w, all_queries(w))
 
 
-def test_all_skipped_rows_give_zero_and_neg_inf():
+@pytest.mark.parametrize("h_q", [16, 64, 128])
+@pytest.mark.parametrize("num_sms", [0, 12])
+def test_all_skipped_rows_give_zero_and_neg_inf(h_q, num_sms):
+    """Query tokens with no valid index give +0 and -inf; partly masked
+    tiles and sub-tiles around them.  Row 1 is all -1; row 3 has its first
+    128-slot tile empty and the second partly valid; row 2 has its first
+    64-token half-tile empty and the second half valid; row 0 has the first
+    half-tile of its third tile empty.  With 12 SMs every query token is
+    split over several parts, so some splits start on an empty half-tile or
+    hold no valid token at all."""
     rng = np.random.default_rng(7)
-    idx = _random_idx(rng, 4, 1, 200, 256)
+    idx = _random_idx(rng, 4, 1, 400, 512)
     idx[1] = -1
     idx[3, 0, :130] = -1          # first tile empty, second partly valid
-    w = _custom(64, 200, 256, idx)
-    out, lse, err = DeviceWorkload(w).run()
+    idx[2, 0, :64] = -1           # first half-tile empty, second half valid
+    idx[0, 0, 256:320] = -1       # third tile: first half empty
+    w = _custom(h_q, 400, 512, idx)
+    out, lse, err = DeviceWorkload(w).run(num_sms=num_sms)
+    assert err == 0
     assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
     assert not torch.signbit(out[1].float()).any()
     compare(out, lse, w, all_queries(w))
@@ -114,23 +126,30 @@ def test_extra_cache_joint_softmax_and_extra_only_rows():
     compare(out, lse, w, all_queries(w))
 
 
-def test_duplicate_indices_count_twice():
+@pytest.mark.parametrize("h_q", [16, 64, 128])
+def test_duplicate_indices_count_twice(h_q):
     rng = np.random.default_rng(9)
     idx = _random_idx(rng, 2, 1, 100, 320)
     idx[:, :, 50:] = idx[:, :, :50]
-    w = _custom(16, 100, 320, idx)
+    w = _custom(h_q, 100, 320, idx)
     out, lse, _ = DeviceWorkload(w).run()
     compare(out, lse, w, all_queries(w))
 
 
-def test_bad_indices_are_skipped_and_flagged():
+@pytest.mark.parametrize("h_q", [32, 64, 128])
+def test_bad_indices_are_skipped_and_flagged(h_q):
+    """Entries past the pool or negative other than -1 are skipped on both
+    sides and flagged; one bad entry sits in the first half-tile, one in the
+    second half of the second tile."""
     rng = np.random.default_rng(10)
     idx = _random_idx(rng, 2, 1, 150, 448)
     idx[0, 0, 5] = 2 * 448 + 7       # past the pool (7 pages per sequence)
     idx[1, 0, 140] = -5              # negative, not -1
-    w = _custom(32, 150, 448, idx)
+    idx[1, 0, 77] = 1 << 30          # far past the pool
+    w = _custom(h_q, 150, 448, idx)
     out, lse, err = DeviceWorkload(w).run()
     assert err & mla.DEVERR_BAD_INDEX
+    assert err & ~mla.DEVERR_BAD_INDEX == 0
     compare(out, lse, w, all_queries(w))
 
 
