@@ -9,32 +9,6 @@
 #include "mla_internal.h"
 
 namespace mla {
-namespace {
-
-constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices] = {0};
-std::mutex g_sm_mutex;
-
-mla_status_t device_sm_count(int* out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-  if (dev >= 0 && dev < kMaxDevices) {
-    std::lock_guard<std::mutex> lock(g_sm_mutex);
-    if (g_sm_count[dev] == 0) {
-      int n = 0;
-      if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
-      g_sm_count[dev] = n;
-    }
-    *out = g_sm_count[dev];
-    return MLA_OK;
-  }
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
-  *out = n;
-  return MLA_OK;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape checks shared by every entry point.
 mla_status_t validate_problem(const mla_problem_t* p) {
@@ -77,6 +51,33 @@ Plan plan_for_parts(const mla_problem_t* p, int num_parts) {
   pl.ws_bytes = pl.ws_o_bytes + static_cast<size_t>(pl.max_splits) * p->h_q * sizeof(float);
   return pl;
 }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+std::mutex g_sm_mutex;
+
+mla_status_t device_sm_count(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lock(g_sm_mutex);
+    if (g_sm_count[dev] == 0) {
+      int n = 0;
+      if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+      g_sm_count[dev] = n;
+    }
+    *out = g_sm_count[dev];
+    return MLA_OK;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+  *out = n;
+  return MLA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Balanced partition: about one part per SM for each head group (a CTA
 // fills an SM), never more parts than work items.

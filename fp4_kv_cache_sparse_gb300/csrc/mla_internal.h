@@ -8,6 +8,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/mla.h"
+
 namespace mla {
 
 // Everything the decode kernel reads, resolved by the host layer.
@@ -41,6 +43,13 @@ struct Plan {
   int64_t max_splits;
   size_t ws_o_bytes, ws_bytes;
 };
+
+// Shape checks shared by every entry point (MLA_OK or the status to return).
+mla_status_t validate_problem(const mla_problem_t* p);
+
+// Shape part of the plan plus the workspace layout (ws_bytes) for a given
+// part count; the one definition of the workspace size.
+Plan plan_for_parts(const mla_problem_t* p, int num_parts);
 
 template <int NH>
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream);

@@ -11,36 +11,24 @@
 // How: the workspace is a file-scope __device__ array of fixed size that the
 // CUDA runtime places on every device that loads this library (it stays
 // there until the process exits).  Host code cannot use the array's name as
-// a device address, so the first call on each device looks its address up
-// with cudaGetSymbolAddress (with that device current) and keeps it; that
-// first call should therefore come before any stream capture.  Every call
-// then runs the ordinary mla_sparse_decode with that address as workspace.
-// The decode writes every partial it later reads, so nothing needs clearing
-// between calls; calls that overlap on the GPU (other streams, other host
-// threads) share the one array and race.
+// a device address, so every call looks the address up with
+// cudaGetSymbolAddress on the current device and passes it on.  Looking it
+// up per call (a host-side query) keeps the address right even after a
+// device reset has rebuilt the context; the first lookup on a device also
+// loads this library's device code there, so that first call should come
+// before any stream capture.  Every call then runs the ordinary
+// mla_sparse_decode with that address as workspace.  The decode writes
+// every partial it later reads, so nothing needs clearing between calls;
+// calls that overlap on the GPU (other streams, other host threads) share
+// the one array and race.
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/mla.h"
+#include "mla_internal.h"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 __device__ __align__(256) unsigned char g_decode_scratch[MLA_NOALLOC_SCRATCH_BYTES];
-
-std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Same upper bound as the workspace mla_get_metadata reports: one slot per
-// query token plus one per part, each h_q x (512 + 1) floats, the output
-// block padded to 256 bytes.
-size_t workspace_bytes(const mla_problem_t* p, int32_t num_parts) {
-  const size_t splits = static_cast<size_t>(p->batch) * p->seq_len_q + static_cast<size_t>(num_parts);
-  size_t o = splits * p->h_q * MLA_HEAD_DIM * sizeof(float);
-  o = (o + 255) & ~size_t(255);
-  return o + splits * p->h_q * sizeof(float);
-}
 
 }  // namespace
 
@@ -49,21 +37,15 @@ extern "C" mla_status_t mla_sparse_decode_noalloc(const mla_problem_t* problem, 
                                                   const int32_t* extra_indices, const int32_t* d_sched,
                                                   const int32_t* d_num_splits, int32_t num_parts, void* out,
                                                   float* lse, int32_t* d_error, mla_stream_t stream) {
-  if (problem == nullptr || num_parts < 1 || problem->batch < 1 || problem->seq_len_q < 1 || problem->h_q < 1)
-    return MLA_ERR_INVALID_ARG;
-  if (workspace_bytes(problem, num_parts) > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  // The problem is checked first, so an invalid or unsupported problem gets
+  // that status and not MLA_ERR_WORKSPACE.
+  const mla_status_t st = mla::validate_problem(problem);
+  if (st != MLA_OK) return st;
+  if (num_parts < 1) return MLA_ERR_INVALID_ARG;
+  // The same workspace size mla_get_metadata reports for this part count.
+  if (mla::plan_for_parts(problem, num_parts).ws_bytes > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-      void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_decode_scratch) != cudaSuccess || addr == nullptr) return MLA_ERR_CUDA;
-      g_scratch_addr[dev] = addr;
-    }
-    scratch = g_scratch_addr[dev];
-  }
+  if (cudaGetSymbolAddress(&scratch, g_decode_scratch) != cudaSuccess || scratch == nullptr) return MLA_ERR_CUDA;
   return mla_sparse_decode(problem, q, kv, indices, extra_kv, extra_indices, d_sched, d_num_splits, num_parts,
                            scratch, MLA_NOALLOC_SCRATCH_BYTES, out, lse, d_error, stream);
 }

@@ -198,13 +198,16 @@ mla_status_t mla_dequantize(int32_t kv_format, const void* records, int64_t n, v
  *
  * Same arguments and result as mla_sparse_decode minus the workspace: the
  * split partials go to a fixed array of MLA_NOALLOC_SCRATCH_BYTES that every
- * device loading this library holds until the process exits.  The first call
- * on a device looks up that array's device address (make it before any stream
- * capture).  Returns MLA_ERR_WORKSPACE, with nothing enqueued, when the
- * problem's workspace (the bytes mla_get_metadata reports for it) exceeds
- * MLA_NOALLOC_SCRATCH_BYTES.  All calls share the one array: calls that
- * overlap on the GPU race and must be serialised by the caller (one stream).
- * Allocates nothing.
+ * device loading this library holds until the process exits.  Every call
+ * looks up that array's address on the current device (a host-side query, so
+ * the address stays right after a device reset); the first lookup on a device
+ * also loads the library's device code there, so make the first call before
+ * any stream capture.  The problem is validated first (MLA_ERR_INVALID_ARG /
+ * MLA_ERR_UNSUPPORTED as for mla_sparse_decode); then MLA_ERR_WORKSPACE, with
+ * nothing enqueued, when the problem's workspace (the bytes mla_get_metadata
+ * reports for it) exceeds MLA_NOALLOC_SCRATCH_BYTES.  All calls share the one
+ * array: calls that overlap on the GPU race and must be serialised by the
+ * caller (one stream).  Allocates nothing.
  */
 #define MLA_NOALLOC_SCRATCH_BYTES (128u * 1024u * 1024u)
 mla_status_t mla_sparse_decode_noalloc(const mla_problem_t* problem,

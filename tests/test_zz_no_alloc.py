@@ -4,8 +4,8 @@ runtime, a serving loop whose memory is all pre-reserved by its own pool).
 Its split partials live in the library's fixed device array instead of a
 caller workspace.  Checked through the C ABI against mla_sparse_decode on
 the same inputs, twice in a row (the array keeps the previous call's
-contents).  Collected last so that a failure here leaves the rest of the
-suite already run."""
+contents), and against the fp64 oracle on sampled query tokens.  Collected
+last so that a failure here leaves the rest of the suite already run."""
 import ctypes
 
 import numpy as np
@@ -14,7 +14,7 @@ import torch
 
 import fp4_kv_cache_sparse_gb300 as mla
 import synth
-from _harness import DeviceWorkload, OUT_ATOL, OUT_RTOL, LSE_ATOL
+from _harness import DeviceWorkload, OUT_ATOL, OUT_RTOL, LSE_ATOL, compare, sample_queries
 
 pytestmark = pytest.mark.gpu
 
@@ -49,16 +49,19 @@ def _close(a_out, a_lse, b_out, b_lse):
     assert torch.all(both | ((a_lse - b_lse).abs() <= LSE_ATOL))
 
 
-@pytest.mark.parametrize("cid", [1, 3])
+@pytest.mark.parametrize("cid", [1, 2, 3])
 def test_noalloc_matches_workspace_entry_point_twice(cid):
+    """64 heads (FP8, and FP8 + FP4 extra cache) and 128 heads with two query
+    tokens per sequence (the 2-CTA kernel and the merge)."""
     lib = _lib()
-    w = synth.make_workload(cid, batch=8, workers=1)
+    w = synth.make_workload(cid, batch=8 if cid != 2 else 4, workers=1)
     dw = DeviceWorkload(w)
     dec = dw.decoder()
     assert dec.num_parts > 1 and dec.ws_bytes <= NOALLOC_MAX     # split partials are used
     ref_out, ref_lse = dec(dw.q, dw.kv, dw.idx, dw.xkv, dw.xidx)
     torch.cuda.synchronize()
     err = torch.zeros((1,), dtype=torch.int32, device=dw.dev)
+    qs, oracle_ref = sample_queries(w, n=3, seed=cid), None
     for _ in range(2):
         out = torch.full_like(ref_out, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
@@ -66,6 +69,7 @@ def test_noalloc_matches_workspace_entry_point_twice(cid):
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         _close(out, lse, ref_out, ref_lse)
+        oracle_ref = compare(out, lse, w, qs, oracle_ref)
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
@@ -78,3 +82,15 @@ def test_noalloc_rejects_problems_beyond_its_array():
     st = lib.mla_sparse_decode_noalloc(ctypes.byref(p), _p(dummy), _p(dummy), _p(dummy), None, None,
                                        _p(dummy), _p(dummy), 76, _p(dummy), _p(dummy), None, None)
     assert st == 3          # MLA_ERR_WORKSPACE, nothing enqueued
+
+
+def test_noalloc_checks_the_problem_before_the_array_size():
+    """An unsupported problem (48 heads) is reported as such, not as a
+    workspace overflow, even when it would also overflow the array."""
+    lib = _lib()
+    p = mla.Problem.make(4096, 1, 48, 2048, 1 << 20)
+    dev = torch.device("cuda", 0)
+    dummy = torch.zeros((16,), dtype=torch.int32, device=dev)
+    st = lib.mla_sparse_decode_noalloc(ctypes.byref(p), _p(dummy), _p(dummy), _p(dummy), None, None,
+                                       _p(dummy), _p(dummy), 76, _p(dummy), _p(dummy), None, None)
+    assert st == 2          # MLA_ERR_UNSUPPORTED, nothing enqueued
