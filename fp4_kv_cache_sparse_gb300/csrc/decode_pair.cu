@@ -179,6 +179,49 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// One elected lane of a converged warp issues (same products as above).
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+// Bounded wait used when the CTA is about to end: it ignores the abort flag
+// (products already issued must complete before TMEM goes away) but gives
+// up after its own limit.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int32_t* d_error) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 63) == 63 && global_timer_ns() - t0 > kWaitNs) {
+      if (d_error) atomicOr(d_error, MLA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -448,115 +491,132 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
   } else if (warp == kIssueWarp) {
     // ------------------------------------------------------------------
-    // Tensor-core issue (one thread): per 64-token sub-tile, S = Q K^T
-    // (A = Q in shared memory, into the S buffer of the sub-tile's parity),
-    // O += P V over this CTA's token quarter once its P is written and over
-    // the peer's once the peer's P has landed, each as soon as it can go.
+    // Tensor-core issue.  The whole warp runs the loop (lane 0 tests the
+    // barriers and broadcasts what it saw, so the warp stays converged) and
+    // one elected lane issues each product: per 64-token sub-tile, S = Q K^T
+    // (A = Q in TMEM, into the S buffer of the sub-tile's parity), O += P V
+    // over this CTA's token quarter once its P is written and over the
+    // peer's once the peer's P has landed, each as soon as it can go.
     // ------------------------------------------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, 256, false, true);
-      const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
-      const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
-      uint32_t n_sub = 0, n_seg = 0;
-      bool issued = false;
-      auto issue_qk = [&](uint32_t nt) {
-        const uint32_t buf = nt % kKvBufs, sb = nt & 1;
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
+    constexpr uint32_t idesc_qk = make_idesc_bf16(128, 64, false, false);
+    constexpr uint32_t idesc_pv = make_idesc_bf16(128, 256, false, true);
+    const uint32_t kv_base = smem_u32(sKV), p_base = smem_u32(sP);
+    const uint32_t tS = tmem + kColS, tO = tmem + kColO, tQ = tmem + kColQ;
+    uint32_t n_sub = 0, n_seg = 0;
+    bool issued = false;
+    auto test = [&](int bar, uint32_t parity) {
+      int ok = 0;
+      if (lane == 0) ok = mbar_test(&bars[bar], parity);
+      return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    };
+    auto issue_qk = [&](uint32_t nt) {
+      const uint32_t buf = nt % kKvBufs, sb = nt & 1;
+      // B descriptor of the first K step; later steps only move the start
+      // address (the 14-bit field cannot carry: shared memory ends below
+      // 256 KB).
+      const uint64_t b0 = make_smem_desc(kv_base + buf * 32768, 16, 1024, kSwizzle128);
+      const uint32_t d = tS + 64 * sb;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t b = make_smem_desc(kv_base + buf * 32768 + k * 8192 + kk * 32, 16, 1024, kSwizzle128);
-            mma_bf16_ts(tS + 64 * sb, tQ + k * 32 + kk * 8, b, idesc_qk, (k | kk) != 0);
+      for (int j = 0; j < 16; ++j)
+        mma_ts_elect(d, tQ + j * 8, b0 + (((j >> 2) * 8192 + (j & 3) * 32) >> 4), idesc_qk, j != 0);
+      commit_elect(&bars[bSFull + sb]);
+    };
+    // O += P V over the 16-token K steps q0, q0+1 (this CTA's quarter or
+    // the peer's) of sub-tile buffer buf: one N = 256 product per step, all
+    // four 64-dim chunks of this CTA's V at once, so P is read once.
+    auto issue_pv = [&](uint32_t buf, uint32_t pb, int q0, bool init) {
+      const uint64_t a0 = make_smem_desc(p_base + pb * 16384 + q0 * 4096, 16, 256, kSwizzle32);
+      const uint64_t b0 = make_smem_desc(kv_base + buf * 32768 + q0 * 2048, 8192, 1024, kSwizzle128);
+      mma_ss_elect(tO, a0, b0, idesc_pv, !init);
+      mma_ss_elect(tO, a0 + (4096 >> 4), b0 + (2048 >> 4), idesc_pv, 1);
+    };
+    for (int64_t g = span.g_begin; g < span.g_end;) {
+      const int qidx = static_cast<int>(g / p.T);
+      const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
+      const uint32_t seg_subs = static_cast<uint32_t>(2 * (seg_end - g));
+      const uint32_t base = n_sub;
+      // Q of this query token is in TMEM once the softmax warps have
+      // written it (after the previous token's epilogue).
+      mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
+      __syncwarp();
+      tc_fence_after();
+      issued = true;
+      // Issue each product of the segment as soon as its inputs are ready:
+      // the second half of O += P V first (it frees a tile buffer for the
+      // dequantizers), then the first half, then the next S = Q K^T (its S
+      // buffer released by the softmax two sub-tiles back, its tile in
+      // shared memory), so that the tensor core works during the softmax.
+      uint32_t qk = 0, pva = 0, pvb = 0;
+      uint64_t idle_since = 0;
+      uint32_t idle_it = 0;
+      bool stop = false;
+      while (pvb < seg_subs && !stop) {
+        bool progress = false;
+        if (pvb < pva) {
+          const uint32_t n = base + pvb, pb = n & 1;
+          if (test(bPIn + pb, (n >> 1) & 1)) {
+            tc_fence_after();
+            issue_pv(n % kKvBufs, pb, 2 * static_cast<int>(peer), false);
+            commit_elect(&bars[bKvFree + n % kKvBufs]);
+            commit_elect(&bars[bPvDone + pb]);
+            if (pvb + 1 == seg_subs) commit_elect(&bars[bOReady]);
+            ++pvb;
+            progress = true;
           }
         }
-        mma_commit(&bars[bSFull + sb]);
-      };
-      // O += P V over the 16-token K steps q0, q0+1 (this CTA's quarter or
-      // the peer's) of sub-tile buffer buf: one N = 256 product per step, all
-      // four 64-dim chunks of this CTA's V at once, so P is read once.
-      auto issue_pv = [&](uint32_t buf, uint32_t pb, int q0, bool init) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int ks = q0 + q;
-          const uint64_t a =
-              make_smem_desc(p_base + pb * 16384 + ks * 4096, 16, 256, kSwizzle32);
-          const uint64_t b = make_smem_desc(kv_base + buf * 32768 + ks * 2048, 8192, 1024, kSwizzle128);
-          mma_bf16_ss(tO, a, b, idesc_pv, !(init && q == 0));
+        if (pva < qk) {
+          const uint32_t n = base + pva;
+          if (test(bPMine2 + (n & 1), (n >> 1) & 1)) {
+            tc_fence_after();
+            issue_pv(n % kKvBufs, n & 1, 2 * static_cast<int>(c), pva == 0);
+            ++pva;
+            progress = true;
+          }
         }
-      };
-      for (int64_t g = span.g_begin; g < span.g_end;) {
-        const int qidx = static_cast<int>(g / p.T);
-        const int64_t seg_end = min(span.g_end, static_cast<int64_t>(qidx + 1) * p.T);
-        const uint32_t seg_subs = static_cast<uint32_t>(2 * (seg_end - g));
-        const uint32_t base = n_sub;
-        // Q of this query token is in shared memory once the softmax warps
-        // have written it (after the previous token's epilogue).
-        mbar_wait(&bars[bQFull], n_seg & 1, abort_flag, p.d_error, kWaitNs);
-        tc_fence_after();
-        issued = true;
-        // Issue each product of the segment as soon as its inputs are ready:
-        // the second half of O += P V first (it frees a tile buffer for the
-        // dequantizers), then the first half, then the next S = Q K^T (its S
-        // buffer released by the softmax two sub-tiles back, its tile in
-        // shared memory), so that the tensor core works during the softmax.
-        uint32_t qk = 0, pva = 0, pvb = 0;
-        const uint64_t t0 = global_timer_ns();
-        for (uint32_t it = 0; pvb < seg_subs; ++it) {
-          bool progress = false;
-          if (pvb < pva) {
-            const uint32_t n = base + pvb, pb = n & 1;
-            if (mbar_test(&bars[bPIn + pb], (n >> 1) & 1)) {
-              tc_fence_after();
-              issue_pv(n % kKvBufs, pb, 2 * static_cast<int>(peer), false);
-              mma_commit(&bars[bKvFree + n % kKvBufs]);
-              mma_commit(&bars[bPvDone + pb]);
-              if (pvb + 1 == seg_subs) mma_commit(&bars[bOReady]);
-              ++pvb;
-              progress = true;
-            }
+        if (qk < seg_subs && qk < pva + 2) {
+          const uint32_t n = base + qk, buf = n % kKvBufs;
+          if ((n < 2 || test(bSUsed + (n & 1), ((n - 2) >> 1) & 1)) && test(bKvFull + buf, (n / kKvBufs) & 1)) {
+            tc_fence_after();
+            issue_qk(n);
+            ++qk;
+            progress = true;
           }
-          if (pva < qk) {
-            const uint32_t n = base + pva;
-            if (mbar_test(&bars[bPMine2 + (n & 1)], (n >> 1) & 1)) {
-              tc_fence_after();
-              issue_pv(n % kKvBufs, n & 1, 2 * static_cast<int>(c), pva == 0);
-              ++pva;
-              progress = true;
-            }
-          }
-          if (qk < seg_subs && qk < pva + 2) {
-            const uint32_t n = base + qk, buf = n % kKvBufs;
-            if ((n < 2 || mbar_test(&bars[bSUsed + (n & 1)], ((n - 2) >> 1) & 1)) &&
-                mbar_test(&bars[bKvFull + buf], (n / kKvBufs) & 1)) {
-              tc_fence_after();
-              issue_qk(n);
-              ++qk;
-              progress = true;
-            }
-          }
-          if (!progress) {
-            __nanosleep(32);
-            if ((it & 63) == 63) {
-              if (*abort_flag) break;
-              if (global_timer_ns() - t0 > kWaitNs) {
+        }
+        if (progress) {
+          idle_it = 0;
+        } else {
+          __nanosleep(32);
+          // The wait limit applies to each stretch without progress.
+          if ((++idle_it & 63) == 1) {
+            int quit = 0;
+            if (lane == 0) {
+              const uint64_t now = global_timer_ns();
+              if (idle_it == 1) idle_since = now;
+              if (*abort_flag) {
+                quit = 1;
+              } else if (now - idle_since > kWaitNs) {
                 *abort_flag = 1;
                 if (p.d_error) atomicOr(p.d_error, MLA_DEVERR_TIMEOUT);
-                break;
+                quit = 1;
               }
             }
+            stop = __shfl_sync(0xFFFFFFFFu, quit, 0) != 0;
           }
         }
-        n_sub = base + seg_subs;
-        g = seg_end;
-        ++n_seg;
       }
-      if (issued) {
-        mma_commit(&bars[bDrain]);
-        mbar_wait(&bars[bDrain], 0, abort_flag, p.d_error, kWaitNs);
-      }
+      n_sub = base + seg_subs;
+      g = seg_end;
+      ++n_seg;
+      if (stop) break;
     }
-    __syncwarp();
+    if (issued) {
+      // Every product issued completes before TMEM is released, even after
+      // a timeout (this wait ignores the abort flag; it has its own bound).
+      commit_elect(&bars[bDrain]);
+      __syncwarp();
+      mbar_wait_drain(&bars[bDrain], 0, p.d_error);
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------------------------------
     // Softmax warps 0-7.  Warp w serves the 32 heads of TMEM lane quadrant
