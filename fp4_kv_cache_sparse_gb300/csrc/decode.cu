@@ -163,6 +163,41 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// One elected lane of a converged warp issues: D[tmem] (+)= A[smem] * B[smem].
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait used when the CTA is about to end: it ignores the abort flag
+// (asynchronous work already issued must complete before TMEM and shared
+// memory go away) but gives up after its own limit.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, int32_t* d_error) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 63) == 63 && global_timer_ns() - t0 > kWaitLimitNs) {
+      if (d_error) atomicOr(d_error, MLA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
 // Work decomposition shared by all roles of a CTA.
 struct Span {
   int64_t g_begin, g_end;
@@ -218,10 +253,11 @@ struct LaneTile {
   bool extra;
 };
 
-__device__ __forceinline__ LaneTile lane_tile(const DecodeParams& p, int64_t g, int row0) {
+__device__ __forceinline__ LaneTile lane_tile(const DecodeParams& p, int g, int row0) {
   LaneTile lt;
-  const int qidx = static_cast<int>(g / p.T);
-  const TileInfo ti = tile_info(p, qidx, static_cast<int>(g - static_cast<int64_t>(qidx) * p.T));
+  // Items number fewer than 2^31 (the host checks), so 32-bit division.
+  const int qidx = g / p.T;
+  const TileInfo ti = tile_info(p, qidx, g - qidx * p.T);
   lt.extra = ti.extra;
 #pragma unroll
   for (int r = 0; r < kRounds; ++r) {
@@ -351,9 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     LaneTile cur{}, nxt{};
     QuarterRegs buf[4];
     if (g < span.g_end) {
-      cur = lane_tile(p, g, row0);
+      cur = lane_tile(p, static_cast<int>(g), row0);
       validate(p, cur, flag_bad);
-      if (g + 1 < span.g_end) nxt = lane_tile(p, g + 1, row0);
+      if (g + 1 < span.g_end) nxt = lane_tile(p, static_cast<int>(g + 1), row0);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) load_quarter(p, cur, qq, seg, buf[qq]);
     }
@@ -375,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool extra = cur.extra;
       LaneTile nxt2{};
-      if (g + 2 < span.g_end) nxt2 = lane_tile(p, g + 2, row0);
+      if (g + 2 < span.g_end) nxt2 = lane_tile(p, static_cast<int>(g + 2), row0);
       if (g + 1 < span.g_end) validate(p, nxt, flag_bad);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
@@ -456,27 +492,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t id = slot < ti.nslots ? __ldg(ti.ids + slot) : -1;
         const bool valid = id >= 0 && static_cast<int64_t>(id) < ti.pool;
 
-        if (tid == 0) {
-          // S^T = K Q^T over the 8 dim chunks, as quarters arrive.
+        if (warp == 0) {
+          // S^T = K Q^T over the 8 dim chunks, as quarters arrive (the whole
+          // warp waits; one elected lane issues).
           if (first) mbar_wait(&bars[kQFull], n_seg & 1, abort_flag, p.d_error, kWaitLimitNs);
 #pragma unroll 1
           for (int qq = 0; qq < 4; ++qq) {
             mbar_wait(&bars[kQuarterFull + qq], n_tile & 1, abort_flag, p.d_error, kWaitLimitNs);
+            __syncwarp();
             tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int c = 2 * qq + cc;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t a = make_smem_desc(kv_base + c * 16384 + k * 32, 16, 1024, kSwizzle128);
-                const uint64_t b = make_smem_desc(q_base + c * (NH * 128) + k * 32, 16, 1024, kSwizzle128);
-                mma_bf16_ss(tmem, a, b, idesc_qk, (c | k) != 0);
-              }
-            }
+            // First K step's descriptors; later steps only move the start
+            // address (the 14-bit field cannot carry below 256 KB).
+            const uint64_t a0 = make_smem_desc(kv_base + 2 * qq * 16384, 16, 1024, kSwizzle128);
+            const uint64_t b0 = make_smem_desc(q_base + 2 * qq * (NH * 128), 16, 1024, kSwizzle128);
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j)
+              mma_ss_elect(tmem, a0 + (((j >> 2) * 16384 + (j & 3) * 32) >> 4),
+                           b0 + (((j >> 2) * NH * 128 + (j & 3) * 32) >> 4), idesc_qk, (qq | j) != 0);
           }
           issued = true;
-          mma_commit(&bars[kSFull]);
-          if (g + 1 == seg_end) mma_commit(&bars[kQFree]);
+          commit_elect(&bars[kSFull]);
+          if (g + 1 == seg_end) commit_elect(&bars[kQFree]);
         }
         mbar_wait(&bars[kSFull], n_tile & 1, abort_flag, p.d_error, kWaitLimitNs);
         __syncwarp();
@@ -608,20 +644,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(1, kSoftmaxThreads);
-        if (tid == 0) {
-          // O^T += V^T P^T.
+        if (warp == 0) {
+          // O^T += V^T P^T (whole warp; one elected lane issues).
           tc_fence_after();
+          const uint64_t pb0 = make_smem_desc(p_base, 16 * p_sbo, p_sbo, p_swz);
 #pragma unroll 1
           for (int r = 0; r < 4; ++r) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t a = make_smem_desc(kv_base + 2 * r * 16384 + ks * 2048, 16384, 1024, kSwizzle128);
-              const uint64_t b = make_smem_desc(p_base + ks * 2 * p_sbo, 16 * p_sbo, p_sbo, p_swz);
-              mma_bf16_ss(tmem + NH + r * NH, a, b, idesc_pv, !(first && ks == 0));
-            }
-            mma_commit(&bars[kQuarterFree + r]);
+            const uint64_t a0 = make_smem_desc(kv_base + 2 * r * 16384, 16384, 1024, kSwizzle128);
+#pragma unroll 2
+            for (int ks = 0; ks < 8; ++ks)
+              mma_ss_elect(tmem + NH + r * NH, a0 + ((ks * 2048) >> 4), pb0 + ((ks * 2 * p_sbo) >> 4), idesc_pv,
+                           !(first && ks == 0));
+            commit_elect(&bars[kQuarterFree + r]);
           }
-          if (g + 1 == seg_end) mma_commit(&bars[kOReady]);
+          if (g + 1 == seg_end) commit_elect(&bars[kOReady]);
         }
       }
 
@@ -689,12 +725,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kSoftmaxThreads);  // O and sm_m reads done before the next token's tiles
       ++n_seg;
     }
-    if (tid == 0 && issued) {
+    if (warp == 0 && issued) {
       // Normal runs have completed every product already (the epilogue
       // waited for it); after a timeout this keeps TMEM alive until the
-      // tensor core is done with it.
-      mma_commit(&bars[kDrain]);
-      mbar_wait(&bars[kDrain], 0, abort_flag, p.d_error, kWaitLimitNs);
+      // tensor core is done with it (the wait ignores the abort flag and
+      // has its own bound).
+      commit_elect(&bars[kDrain]);
+      __syncwarp();
+      mbar_wait_drain(&bars[kDrain], 0, p.d_error);
     }
   }
 

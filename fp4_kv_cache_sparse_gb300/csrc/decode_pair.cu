@@ -419,6 +419,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         sc_cur[j] = sc_nxt[j];
       }
     }
+    // The gathers of the last slots land before this CTA's shared memory
+    // goes away, even after a timeout (normally they completed long ago).
+    if (lane == 0) {
+      for (uint32_t k = 0; k < kStgSlots && k < n_chunk; ++k) {
+        const uint32_t i = n_chunk - 1 - k;
+        mbar_wait_drain(&bars[bStgFull + i % kStgSlots], (i / kStgSlots) & 1, p.d_error);
+      }
+    }
+    __syncwarp();
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------------
     // Dequantizers: staging slot (32 tokens x this CTA's 256 dims, raw e4m3)
