@@ -73,6 +73,10 @@ def _load():
     lib.oracle_sparse_mla_decode.restype = ctypes.c_longlong
     lib.oracle_combine.argtypes = [ctypes.c_int, ctypes.c_longlong, P, P, P, P]
     lib.oracle_combine.restype = None
+    lib.oracle_rope_rotate.argtypes = [P, ctypes.c_longlong, P, ctypes.c_double, ctypes.c_int]
+    lib.oracle_rope_rotate.restype = None
+    lib.oracle_rope_fp8_epilogue.argtypes = [P, ctypes.c_longlong, P, ctypes.c_double, P]
+    lib.oracle_rope_fp8_epilogue.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
     _lib = lib
@@ -196,6 +200,36 @@ def combine(o_part: np.ndarray, lse_part: np.ndarray):
     lse = np.empty((rows,), dtype=np.float64)
     _load().oracle_combine(n, rows, _ptr(o), _ptr(l), _ptr(out), _ptr(lse))
     return out, lse
+
+
+def _row_positions(x: np.ndarray, pos) -> np.ndarray:
+    """One int32 position per 512-wide row of x: pos broadcast over x's
+    leading axes (e.g. [b, s] positions for [b, s, h, 512] outputs)."""
+    lead = x.shape[:-1]
+    p = np.asarray(pos, dtype=np.int64)
+    p = p.reshape(p.shape + (1,) * (len(lead) - p.ndim))
+    return np.ascontiguousarray(np.broadcast_to(p, lead).astype(np.int32)).reshape(-1)
+
+
+def rope_rotate(x: np.ndarray, pos, theta: float, sign: int = -1) -> np.ndarray:
+    """Rotary rotation of dims 448..511 of float64 rows [..., 512]: sign -1
+    is the output side's conjugate rotation, +1 the forward one."""
+    v = np.ascontiguousarray(x, dtype=np.float64).copy()
+    rows = v.size // D
+    p = _row_positions(v, pos)
+    _load().oracle_rope_rotate(_ptr(v), rows, _ptr(p), float(theta), int(sign))
+    return v
+
+
+def rope_fp8_epilogue(o: np.ndarray, pos, theta: float) -> np.ndarray:
+    """The fused epilogue: conjugate rotation of float64 outputs [..., 512]
+    and the cast to 528-byte FP8 records [..., 528]."""
+    v = np.ascontiguousarray(o, dtype=np.float64)
+    rows = v.size // D
+    p = _row_positions(v, pos)
+    recs = np.empty(v.shape[:-1] + (FP8_RECORD_BYTES,), dtype=np.uint8)
+    _load().oracle_rope_fp8_epilogue(_ptr(v), rows, _ptr(p), float(theta), _ptr(recs))
+    return recs
 
 
 def num_threads() -> int:

@@ -410,6 +410,47 @@ void oracle_combine(int n_splits, long long rows, const double* o_part, const do
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Output-side epilogue of the fused kernel.                                 */
+/* ------------------------------------------------------------------------ */
+
+/* "deepseek-ai/FlashMLA", "What it is": the fused kernel ends with the
+ * conjugate RoPE on the output side and the cast to FP8 (outputs ready for a
+ * downstream FP8 einsum); "flops/attn-mla-kernel-support-matrix", "notes":
+ * qk_rope_head_dim = 64.  Readings (the pages fix none of them): the rotary
+ * part is the last 64 of the 512 output dims, taken as 32 interleaved pairs
+ * (448 + 2j, 449 + 2j); pair j of a row at position pos turns by
+ * phi_j = pos * theta^(-2j/64); a rotation by sign * phi_j maps (a, b) to
+ * (a cos - b sin, a sin + b cos) of that angle, and the output side applies
+ * the conjugate one (sign = -1).  pos holds one position per row.  Dims
+ * below 448 are not touched. */
+void oracle_rope_rotate(double* x, long long rows, const int32_t* pos, double theta, int sign) {
+    for (long long r = 0; r < rows; ++r) {
+        double* v = x + r * ORACLE_D;
+        for (int j = 0; j < 32; ++j) {
+            const double phi = (double)sign * (double)pos[r] * pow(theta, -2.0 * j / 64.0);
+            const double c = cos(phi), s = sin(phi);
+            const double a = v[448 + 2 * j], b = v[449 + 2 * j];
+            v[448 + 2 * j] = a * c - b * s;
+            v[449 + 2 * j] = a * s + b * c;
+        }
+    }
+}
+
+/* The epilogue: each row of o (the attention output, unrounded) turned by
+ * the conjugate rotation, then cast to FP8 as a 528-byte record in the
+ * cache's own format with the writer's block-scale rule (the FP8 einsum's
+ * block scales: one e8m0 scale per 32 values, a reading). */
+void oracle_rope_fp8_epilogue(const double* o, long long rows, const int32_t* pos, double theta, uint8_t* recs) {
+#pragma omp parallel for schedule(static)
+    for (long long r = 0; r < rows; ++r) {
+        double x[ORACLE_D];
+        memcpy(x, o + r * ORACLE_D, sizeof(x));
+        oracle_rope_rotate(x, 1, pos + r, theta, -1);
+        oracle_encode_fp8_record(x, recs + r * ORACLE_FP8_REC);
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

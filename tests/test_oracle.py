@@ -486,3 +486,78 @@ def test_encoders_agree_with_the_test_input_quantizer():
     x = oracle.bf16_to_f64(synth.f32_to_bf16_bits(x)).astype(np.float32)
     assert np.array_equal(oracle.encode_fp8(x), synth.encode_fp8_records(x))
     assert np.array_equal(oracle.encode_fp4(x), synth.encode_fp4_records(x))
+
+
+# --------------------------------------------------------------------------
+# Output-side epilogue: conjugate rotary embedding of dims 448..511 and the
+# FP8 cast ("deepseek-ai/FlashMLA", "What it is"; qk_rope_head_dim = 64 on
+# "flops/attn-mla-kernel-support-matrix", "notes").  Which dims, the pairing
+# and the frequency rule are readings; these pins check that what is built
+# is a rotation with the stated convention, not the arithmetic retyped.
+# --------------------------------------------------------------------------
+
+THETA = 10000.0
+
+
+def _rows(n, seed):
+    return np.random.default_rng(seed).standard_normal((n, D))
+
+
+def test_rope_position_zero_is_the_identity():
+    x = _rows(6, 1)
+    assert _same(oracle.rope_rotate(x, np.zeros(6, dtype=np.int64), THETA, -1), x)
+    recs = oracle.rope_fp8_epilogue(x, np.zeros(6, dtype=np.int64), THETA)
+    assert np.array_equal(recs, oracle.encode_fp8(x))
+
+
+def test_rope_conjugate_undoes_the_forward_rotation_and_keeps_pair_norms():
+    x = _rows(8, 2)
+    pos = np.array([1, 17, 4095, 65536, 131071, 7, 0, 100000])
+    y = oracle.rope_rotate(x, pos, THETA, -1)
+    back = oracle.rope_rotate(y, pos, THETA, +1)
+    assert np.abs(back - x).max() < 1e-12
+    assert _same(y[:, :448], x[:, :448])               # only the last 64 dims turn
+    nx = np.hypot(x[:, 448::2], x[:, 449::2])
+    ny = np.hypot(y[:, 448::2], y[:, 449::2])
+    assert np.abs(nx - ny).max() < 1e-12               # each pair is rotated, not scaled
+
+
+def test_rope_angles_add():
+    """Turning by position p1 and then p2 is turning by p1 + p2 (what makes
+    it a rotary position encoding); a sign slip in one term breaks this."""
+    x = _rows(4, 3)
+    p1, p2 = np.array([3, 100, 2048, 9]), np.array([5, 28, 999, 40000])
+    two = oracle.rope_rotate(oracle.rope_rotate(x, p1, THETA, -1), p2, THETA, -1)
+    one = oracle.rope_rotate(x, p1 + p2, THETA, -1)
+    assert np.abs(two - one).max() < 1e-9
+
+
+def test_rope_frequencies_of_pairs_0_and_16():
+    """Pair 0 turns by pos radians (theta^0 = 1); pair 16 by pos * theta^-1/2,
+    i.e. 1 radian at pos 100 for theta = 10^4; the conjugate side turns
+    clockwise: (1, 0) -> (cos phi, -sin phi)."""
+    x = np.zeros((2, D))
+    x[:, 448] = 1.0            # pair 0
+    x[:, 448 + 32] = 1.0       # pair 16
+    y = oracle.rope_rotate(x, np.array([1, 100]), THETA, -1)
+    assert abs(y[0, 448] - math.cos(1.0)) < 1e-15 and abs(y[0, 449] + math.sin(1.0)) < 1e-15
+    assert abs(y[1, 480] - math.cos(1.0)) < 1e-12 and abs(y[1, 481] + math.sin(1.0)) < 1e-12
+
+
+def test_rope_fp8_records_decode_to_the_rotated_rows_within_one_step():
+    x = _rows(16, 4) * np.logspace(-3, 3, 16)[:, None]
+    pos = np.arange(16) * 977
+    recs = oracle.rope_fp8_epilogue(x, pos, THETA)
+    y = oracle.rope_rotate(x, pos, THETA, -1)
+    got = oracle.dequant_fp8(recs.reshape(-1, 528)).reshape(y.shape)
+    # Per 32-value block the scale is the least power of two 2^e bringing the
+    # block maximum within 448; an e4m3 value then lies within half a step
+    # (2^(floor(log2|v|) - 4), at least 2^-10 in scaled units) of the input.
+    for r in range(16):
+        for blk in range(16):
+            v = y[r, 32 * blk:32 * blk + 32]
+            e = int(recs[r, 512 + blk]) - 127
+            s = np.abs(v) * 2.0 ** -e
+            half = np.where(s > 0, 2.0 ** (np.floor(np.log2(np.maximum(s, 1e-300))) - 4), 0)
+            half = np.maximum(half, 2.0 ** -10)
+            assert np.all(np.abs(got[r, 32 * blk:32 * blk + 32] * 2.0 ** -e - v * 2.0 ** -e) <= half + 1e-15)
