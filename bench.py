@@ -184,6 +184,30 @@ def time_decode(dw, dec, steps, warmup, flush, dev_barrier=None):
     return ms, t0, t1
 
 
+def time_rope_fp8(dw, dec, steps, warmup, flush):
+    """The decode step with the fused output epilogue (conjugate rotary
+    embedding of dims 448..511 and the cast to FP8 records) on the same
+    workload: CUDA-event time per call, L2 flushed between calls."""
+    b, s = dw.q.shape[0], dw.q.shape[1]
+    pos = torch.arange(b * s, dtype=torch.int32, device=dw.q.device).view(b, s) * 977 % 131072
+    out = torch.empty((b, s, dw.q.shape[2], 528), dtype=torch.uint8, device=dw.q.device)
+    lse = torch.empty((b, s, dw.q.shape[2]), dtype=torch.float32, device=dw.q.device)
+    for _ in range(warmup):
+        dec.rope_fp8(dw.q, dw.kv, dw.idx, pos, 10000.0, dw.xkv, dw.xidx, out=out, lse=lse)
+    stream = torch.cuda.current_stream()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dec.rope_fp8(dw.q, dw.kv, dw.idx, pos, 10000.0, dw.xkv, dw.xidx, out=out, lse=lse)
+        e.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(e))
+    return statistics.mean(ms) * 1e-3
+
+
 def time_kv_writer(dev, pk, steps, warmup, flush, tokens=1 << 20):
     """The KV-cache writer (mla_kv_write) on `tokens` new tokens scattered to
     a random permutation of the pool's slots, FP8 and FP4: CUDA-event time
@@ -440,6 +464,10 @@ def main():
     per_rank_achieved = flops / step_s / 1e12 if bound == "tensor" else kvb / step_s / 1e9
     traffic = profiled_traffic(w.cfg.name)
     metadata_us = time_metadata(dec.problem, dev)
+    rope_s = time_rope_fp8(dw, dec, max(20, args.steps // 20), args.warmup, flush)
+    rope_fp8 = {"us": round(rope_s * 1e6, 2), "tflops": round(flops / rope_s / 1e12, 2),
+                "roofline_frac": round(roofline_of(flops, kvb, rope_s, pk)[1], 4),
+                "step": "mla_sparse_decode_rope_fp8: decode kernel + merge with conjugate RoPE and FP8 cast"}
 
     per_config = {}
     kv_writer = None
@@ -491,6 +519,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 if dec_parts > 1 else 1) * args.steps,
         "metadata_us": round(metadata_us, 1),
+        "rope_fp8": rope_fp8,
         "clocks": clocks.summary(t0, t1) if clocks else None,
         "cpu_baseline": cpu,
         "per_config": per_config,

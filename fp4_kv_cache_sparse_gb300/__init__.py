@@ -16,7 +16,8 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "MLAError", "Problem", "load", "get_metadata", "sparse_decode", "combine", "dequantize", "kv_write",
+    "MLAError", "Problem", "load", "get_metadata", "sparse_decode", "sparse_decode_rope_fp8", "combine",
+    "dequantize", "kv_write",
     "SparseMLADecoder", "decode", "KV_NONE", "KV_FP8_528", "KV_FP4_288", "KV_BF16",
     "DEVERR_BAD_INDEX", "DEVERR_TIMEOUT", "DEVERR_BAD_METADATA", "SCHED_INTS",
 ]
@@ -77,12 +78,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     PP = ctypes.POINTER(Problem)
     lib.mla_get_metadata.argtypes = [PP, I32, P, P, ctypes.POINTER(I32), ctypes.POINTER(SZ), P]
     lib.mla_sparse_decode.argtypes = [PP, P, P, P, P, P, P, P, I32, P, SZ, P, P, P, P]
+    lib.mla_sparse_decode_rope_fp8.argtypes = [PP, P, P, P, P, P, P, P, I32, P, SZ, P, ctypes.c_float, P, P, P, P]
     lib.mla_combine.argtypes = [PP, P, P, P, P, P, P]
     lib.mla_dequantize.argtypes = [I32, P, I64, P, P]
     lib.mla_kv_write.argtypes = [I32, P, P, I64, P, I64, P, P]
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
-    for f in (lib.mla_get_metadata, lib.mla_sparse_decode, lib.mla_combine, lib.mla_dequantize, lib.mla_kv_write):
+    for f in (lib.mla_get_metadata, lib.mla_sparse_decode, lib.mla_sparse_decode_rope_fp8, lib.mla_combine,
+              lib.mla_dequantize, lib.mla_kv_write):
         f.restype = ctypes.c_int
     if path == _build.LIB:
         _lib = lib
@@ -135,6 +138,20 @@ def sparse_decode(problem: Problem, q, kv, indices, sched, num_splits, num_parts
                                  _ptr(out), _ptr(lse), _ptr(error), _stream(stream)), "mla_sparse_decode")
 
 
+def sparse_decode_rope_fp8(problem: Problem, q, kv, indices, sched, num_splits, num_parts, workspace,
+                           positions, rope_theta, out_fp8, lse, extra_kv=None, extra_indices=None, error=None,
+                           stream=None):
+    """The decode step with the fused output epilogue: conjugate rotary
+    embedding of dims 448..511 and the cast to 528-byte FP8 records
+    (out_fp8 uint8 [b, s, h, 528]); positions int32 [b, s]."""
+    lib = load()
+    _check(lib.mla_sparse_decode_rope_fp8(ctypes.byref(problem), _ptr(q), _ptr(kv), _ptr(indices), _ptr(extra_kv),
+                                          _ptr(extra_indices), _ptr(sched), _ptr(num_splits), num_parts,
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _ptr(positions), float(rope_theta), _ptr(out_fp8), _ptr(lse),
+                                          _ptr(error), _stream(stream)), "mla_sparse_decode_rope_fp8")
+
+
 def combine(problem: Problem, num_splits, o_partial, lse_partial, out, lse, stream=None):
     lib = load()
     _check(lib.mla_combine(ctypes.byref(problem), _ptr(num_splits), _ptr(o_partial), _ptr(lse_partial),
@@ -183,6 +200,18 @@ class SparseMLADecoder:
             lse = torch.empty((p.batch, p.seq_len_q, p.h_q), dtype=torch.float32, device=q.device)
         sparse_decode(p, q, kv, indices, self.sched, self.num_splits, self.num_parts, self.workspace,
                       out, lse, extra_kv, extra_indices, self.error, stream)
+        return out, lse
+
+    def rope_fp8(self, q, kv, indices, positions, rope_theta=10000.0, extra_kv=None, extra_indices=None,
+                 out=None, lse=None, stream=None):
+        """Decode with the fused epilogue; returns (FP8 records uint8 [b, s, h, 528], lse)."""
+        p = self.problem
+        if out is None:
+            out = torch.empty((p.batch, p.seq_len_q, p.h_q, FP8_RECORD_BYTES), dtype=torch.uint8, device=q.device)
+        if lse is None:
+            lse = torch.empty((p.batch, p.seq_len_q, p.h_q), dtype=torch.float32, device=q.device)
+        sparse_decode_rope_fp8(p, q, kv, indices, self.sched, self.num_splits, self.num_parts, self.workspace,
+                               positions, rope_theta, out, lse, extra_kv, extra_indices, self.error, stream)
         return out, lse
 
 

@@ -93,6 +93,85 @@ Plan make_plan(const mla_problem_t* p, int num_sms) {
 }
 
 }  // namespace
+
+// Validation and the decode kernel's launch, shared by the bf16 and the
+// FP8 output calls.  With force_partials every query token's result goes
+// to the workspace (out may then be null); *pout receives the parameters.
+mla_status_t decode_launch(const mla_problem_t* problem, const void* q, const void* kv, const int32_t* indices,
+                           const void* extra_kv, const int32_t* extra_indices, const int32_t* d_sched,
+                           const int32_t* d_num_splits, int32_t num_parts, void* workspace, size_t workspace_bytes,
+                           uint16_t* out, float* lse, int32_t* d_error, bool force_partials, mla_stream_t stream,
+                           DecodeParams* pout) {
+  mla_status_t st = validate_problem(problem);
+  if (st != MLA_OK) return st;
+  if (q == nullptr || kv == nullptr || indices == nullptr || d_sched == nullptr || d_num_splits == nullptr ||
+      lse == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(indices) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (problem->extra_topk > 0) {
+    if (extra_kv == nullptr || extra_indices == nullptr || !aligned16(extra_kv) ||
+        (reinterpret_cast<uintptr_t>(extra_indices) & 3u))
+      return MLA_ERR_INVALID_ARG;
+  }
+  // The part ranges live in d_sched (checked on the device); the host needs
+  // only the part count for the grid and the workspace layout.
+  Plan pl = plan_for_parts(problem, num_parts);
+  if (num_parts < 1 || num_parts > pl.G) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < pl.ws_bytes) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int nq = problem->batch * problem->seq_len_q;
+
+  DecodeParams& p = *pout;
+  p = DecodeParams{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv = static_cast<const uint8_t*>(kv);
+  p.idx = indices;
+  p.xkv = problem->extra_topk > 0 ? static_cast<const uint8_t*>(extra_kv) : nullptr;
+  p.xidx = problem->extra_topk > 0 ? extra_indices : nullptr;
+  p.sched = d_sched;
+  p.num_splits = d_num_splits;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_o_bytes);
+  p.ws_splits_cap = pl.max_splits;
+  p.out = out;
+  p.lse = lse;
+  p.d_error = d_error;
+  p.nq = nq;
+  p.h_q = problem->h_q;
+  p.n_hg = pl.n_hg;
+  p.topk = problem->topk;
+  p.xtopk = problem->extra_topk;
+  p.Tm = pl.Tm;
+  p.T = pl.T;
+  const int64_t cap = int64_t(1) << 31;
+  p.pool_tokens = problem->num_pages * MLA_PAGE_SIZE < cap ? problem->num_pages * MLA_PAGE_SIZE : cap;
+  p.xpool_tokens = problem->extra_topk > 0
+                       ? (problem->extra_num_pages * MLA_PAGE_SIZE < cap ? problem->extra_num_pages * MLA_PAGE_SIZE
+                                                                          : cap)
+                       : 0;
+  p.scale_log2 = problem->sm_scale * 1.4426950408889634f;
+  p.force_partials = force_partials ? 1 : 0;
+
+  const int grid = pl.num_parts * pl.n_hg;
+  cudaError_t e;
+  if (problem->h_q == 128 && problem->extra_topk == 0) {
+    // All 128 heads on the MMA's M dimension, the latent dims split over a
+    // 2-CTA cluster (same part count and SM budget as two 64-head groups).
+    e = launch_decode_pair(p, pl.num_parts, s);
+  } else {
+    switch (pl.nh) {
+      case 64: e = launch_decode<64>(p, grid, s); break;
+      case 32: e = launch_decode<32>(p, grid, s); break;
+      default: e = launch_decode<16>(p, grid, s); break;
+    }
+  }
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 }  // namespace mla
 
 using namespace mla;
@@ -139,75 +218,42 @@ mla_status_t mla_sparse_decode(const mla_problem_t* problem, const void* q, cons
                                mla_stream_t stream) {
   mla_status_t st = validate_problem(problem);
   if (st != MLA_OK) return st;
-  if (q == nullptr || kv == nullptr || indices == nullptr || d_sched == nullptr || d_num_splits == nullptr ||
-      out == nullptr || lse == nullptr)
-    return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
-      (reinterpret_cast<uintptr_t>(indices) & 3u))
-    return MLA_ERR_INVALID_ARG;
-  if (problem->extra_topk > 0) {
-    if (extra_kv == nullptr || extra_indices == nullptr || !aligned16(extra_kv) ||
-        (reinterpret_cast<uintptr_t>(extra_indices) & 3u))
-      return MLA_ERR_INVALID_ARG;
-  }
-  // The part ranges live in d_sched (checked on the device); the host needs
-  // only the part count for the grid and the workspace layout.
-  Plan pl = plan_for_parts(problem, num_parts);
-  if (num_parts < 1 || num_parts > pl.G) return MLA_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < pl.ws_bytes) return MLA_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return MLA_ERR_INVALID_ARG;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int nq = problem->batch * problem->seq_len_q;
-
+  if (out == nullptr || !aligned16(out)) return MLA_ERR_INVALID_ARG;
   DecodeParams p{};
-  p.q = static_cast<const uint16_t*>(q);
-  p.kv = static_cast<const uint8_t*>(kv);
-  p.idx = indices;
-  p.xkv = problem->extra_topk > 0 ? static_cast<const uint8_t*>(extra_kv) : nullptr;
-  p.xidx = problem->extra_topk > 0 ? extra_indices : nullptr;
-  p.sched = d_sched;
-  p.num_splits = d_num_splits;
-  p.ws_o = static_cast<float*>(workspace);
-  p.ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_o_bytes);
-  p.ws_splits_cap = pl.max_splits;
-  p.out = static_cast<uint16_t*>(out);
-  p.lse = lse;
-  p.d_error = d_error;
-  p.nq = nq;
-  p.h_q = problem->h_q;
-  p.n_hg = pl.n_hg;
-  p.topk = problem->topk;
-  p.xtopk = problem->extra_topk;
-  p.Tm = pl.Tm;
-  p.T = pl.T;
-  const int64_t cap = int64_t(1) << 31;
-  p.pool_tokens = problem->num_pages * MLA_PAGE_SIZE < cap ? problem->num_pages * MLA_PAGE_SIZE : cap;
-  p.xpool_tokens = problem->extra_topk > 0
-                       ? (problem->extra_num_pages * MLA_PAGE_SIZE < cap ? problem->extra_num_pages * MLA_PAGE_SIZE
-                                                                          : cap)
-                       : 0;
-  p.scale_log2 = problem->sm_scale * 1.4426950408889634f;
-
-  const int grid = pl.num_parts * pl.n_hg;
-  cudaError_t e;
-  if (problem->h_q == 128 && problem->extra_topk == 0) {
-    // All 128 heads on the MMA's M dimension, the latent dims split over a
-    // 2-CTA cluster (same part count and SM budget as two 64-head groups).
-    e = launch_decode_pair(p, pl.num_parts, s);
-  } else {
-    switch (pl.nh) {
-      case 64: e = launch_decode<64>(p, grid, s); break;
-      case 32: e = launch_decode<32>(p, grid, s); break;
-      default: e = launch_decode<16>(p, grid, s); break;
-    }
-  }
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
-  if (pl.num_parts > 1) {
+  st = decode_launch(problem, q, kv, indices, extra_kv, extra_indices, d_sched, d_num_splits, num_parts, workspace,
+                     workspace_bytes, static_cast<uint16_t*>(out), lse, d_error, false, stream, &p);
+  if (st != MLA_OK) return st;
+  if (num_parts > 1) {
     // Only query tokens with more than one split have partials to merge;
     // the kernel skips the others.
-    e = launch_combine(d_num_splits, p.ws_o, p.ws_lse, p.out, lse, nq, problem->h_q, true, s);
-    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    if (launch_combine(d_num_splits, p.ws_o, p.ws_lse, p.out, lse, p.nq, problem->h_q, true,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return MLA_ERR_CUDA;
   }
+  return MLA_OK;
+}
+
+mla_status_t mla_sparse_decode_rope_fp8(const mla_problem_t* problem, const void* q, const void* kv,
+                                        const int32_t* indices, const void* extra_kv, const int32_t* extra_indices,
+                                        const int32_t* d_sched, const int32_t* d_num_splits, int32_t num_parts,
+                                        void* workspace, size_t workspace_bytes, const int32_t* positions,
+                                        float rope_theta, void* out_fp8, float* lse, int32_t* d_error,
+                                        mla_stream_t stream) {
+  mla_status_t st = validate_problem(problem);
+  if (st != MLA_OK) return st;
+  if (out_fp8 == nullptr || positions == nullptr || (reinterpret_cast<uintptr_t>(positions) & 3u) ||
+      (reinterpret_cast<uintptr_t>(out_fp8) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(rope_theta) || !(rope_theta > 1.f)) return MLA_ERR_INVALID_ARG;
+  DecodeParams p{};
+  st = decode_launch(problem, q, kv, indices, extra_kv, extra_indices, d_sched, d_num_splits, num_parts, workspace,
+                     workspace_bytes, nullptr, lse, d_error, true, stream, &p);
+  if (st != MLA_OK) return st;
+  RopeFreqs f{};
+  for (int j = 0; j < 32; ++j) f.f[j] = std::pow(static_cast<double>(rope_theta), -2.0 * j / 64.0);
+  if (launch_rope_fp8(d_num_splits, p.ws_o, p.ws_lse, positions, f, static_cast<uint8_t*>(out_fp8), lse, p.nq,
+                      problem->h_q, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
   return MLA_OK;
 }
 

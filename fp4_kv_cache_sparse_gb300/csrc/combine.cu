@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "mla_device.cuh"
 #include "mla_internal.h"
 
 namespace mla {
@@ -32,6 +33,62 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The merged output of one (query token, head) row: lane l ends with dims
+// 128 k + 4 l .. 128 k + 4 l + 3 in acc[4 k .. 4 k + 3]; returns the row's
+// log-sum-exp (natural log; -inf when every split is empty, acc all zero).
+__device__ __forceinline__ float merge_row(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                                           int s0, int n, int h, int h_q, int lane, float (&acc)[16]) {
+  const float* lrow = lse_part + static_cast<int64_t>(s0) * h_q + h;
+  // Max and sum over the splits, lanes striding over them.
+  float mx = -INFINITY;
+  for (int i = lane; i < n; i += 32) mx = fmaxf(mx, lrow[static_cast<int64_t>(i) * h_q]);
+  const float M = warp_max(mx);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  if (M == -INFINITY) return -INFINITY;
+  float z = 0.f;
+  for (int i = lane; i < n; i += 32) {
+    const float li = lrow[static_cast<int64_t>(i) * h_q];
+    z += li == -INFINITY ? 0.f : expf(li - M);
+  }
+  const float L = M + logf(warp_sum(z));
+  const float* orow = o_part + (static_cast<int64_t>(s0) * h_q + h) * 512;
+  const int64_t ostride = static_cast<int64_t>(h_q) * 512;
+  for (int c = 0; c < n; c += 32) {
+    // Weight of split c + lane, held by that lane; -inf partials weigh 0.
+    float wl = 0.f;
+    if (c + lane < n) {
+      const float li = lrow[static_cast<int64_t>(c + lane) * h_q];
+      wl = li == -INFINITY ? 0.f : expf(li - L);
+    }
+    const int m = min(32, n - c);
+    for (int j = 0; j < m; j += 2) {
+      float4 v[2][4];
+      float w[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        w[u] = __shfl_sync(kFull, wl, (j + u) & 31);
+        const bool use = j + u < m && w[u] != 0.f;
+        const float4* src = reinterpret_cast<const float4*>(orow + (c + j + u) * ostride);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[u][k] = use ? src[k * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!use) w[u] = 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[4 * k + 0] += w[u] * v[u][k].x;
+          acc[4 * k + 1] += w[u] * v[u][k].y;
+          acc[4 * k + 2] += w[u] * v[u][k].z;
+          acc[4 * k + 3] += w[u] * v[u][k].w;
+        }
+      }
+    }
+  }
+  return L;
+}
+
 __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* __restrict__ num_splits,
                                                              const float* __restrict__ o_part,
                                                              const float* __restrict__ lse_part,
@@ -49,58 +106,8 @@ __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* 
   const int s0 = num_splits[qidx];
   const int n = num_splits[qidx + 1] - s0;
   if (skip_single && n == 1) return;
-  const float* lrow = lse_part + static_cast<int64_t>(s0) * h_q + h;
-
-  // Max and sum over the splits, lanes striding over them.
-  float mx = -INFINITY;
-  for (int i = lane; i < n; i += 32) mx = fmaxf(mx, lrow[static_cast<int64_t>(i) * h_q]);
-  const float M = warp_max(mx);
   float acc[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  float L = -INFINITY;
-  if (M != -INFINITY) {
-    float z = 0.f;
-    for (int i = lane; i < n; i += 32) {
-      const float li = lrow[static_cast<int64_t>(i) * h_q];
-      z += li == -INFINITY ? 0.f : expf(li - M);
-    }
-    L = M + logf(warp_sum(z));
-    const float* orow = o_part + (static_cast<int64_t>(s0) * h_q + h) * 512;
-    const int64_t ostride = static_cast<int64_t>(h_q) * 512;
-    for (int c = 0; c < n; c += 32) {
-      // Weight of split c + lane, held by that lane; -inf partials weigh 0.
-      float wl = 0.f;
-      if (c + lane < n) {
-        const float li = lrow[static_cast<int64_t>(c + lane) * h_q];
-        wl = li == -INFINITY ? 0.f : expf(li - L);
-      }
-      const int m = min(32, n - c);
-      for (int j = 0; j < m; j += 2) {
-        float4 v[2][4];
-        float w[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          w[u] = __shfl_sync(kFull, wl, (j + u) & 31);
-          const bool use = j + u < m && w[u] != 0.f;
-          const float4* src = reinterpret_cast<const float4*>(orow + (c + j + u) * ostride);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) v[u][k] = use ? src[k * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!use) w[u] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            acc[4 * k + 0] += w[u] * v[u][k].x;
-            acc[4 * k + 1] += w[u] * v[u][k].y;
-            acc[4 * k + 2] += w[u] * v[u][k].z;
-            acc[4 * k + 3] += w[u] * v[u][k].w;
-          }
-        }
-      }
-    }
-  }
+  const float L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
   uint2* dst = reinterpret_cast<uint2*>(out + row * 512);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -110,6 +117,63 @@ __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* 
     w.x = *reinterpret_cast<const uint32_t*>(&a);
     w.y = *reinterpret_cast<const uint32_t*>(&b);
     dst[k * 32 + lane] = w;
+  }
+  if (lane == 0) lse[row] = L;
+}
+
+// The fused output epilogue ("deepseek-ai/FlashMLA", "What it is": the
+// conjugate RoPE on the output side and the cast to FP8).  Every query
+// token's splits (one or more) are merged as above; then dims 448..511 (the
+// rotary part: 32 interleaved pairs, held by lanes 16..31 in acc[12..15])
+// turn by -phi_j, phi_j = pos * theta^(-2j/64), the angle taken in double
+// and reduced to [-pi, pi] before the float sine and cosine; then each
+// 32-dim block (eight lanes) is cast to E4M3FN under its e8m0 scale, giving
+// a 528-byte record per row in the cache's own format.
+__global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t* __restrict__ num_splits,
+                                                              const float* __restrict__ o_part,
+                                                              const float* __restrict__ lse_part,
+                                                              const int32_t* __restrict__ positions,
+                                                              const RopeFreqs freqs, uint8_t* __restrict__ out,
+                                                              float* __restrict__ lse, int nq, int h_q) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= static_cast<int64_t>(nq) * h_q) return;  // whole warps leave together
+  const int qidx = static_cast<int>(row / h_q);
+  const int h = static_cast<int>(row % h_q);
+  const int s0 = num_splits[qidx];
+  const int n = num_splits[qidx + 1] - s0;
+  float acc[16];
+  const float L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
+  if (lane >= 16) {
+    const double pos = static_cast<double>(positions[qidx]);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = 2 * (lane - 16) + u;  // pair (448 + 2j, 449 + 2j)
+      double phi = pos * freqs.f[j];
+      phi -= 6.283185307179586 * rint(phi * 0.15915494309189535);
+      // |phi| <= pi here, where the fast sine and cosine are within
+      // 2^-21 absolute: far below one E4M3 step of the result.
+      float sn, cs;
+      __sincosf(static_cast<float>(phi), &sn, &cs);
+      const float a = acc[12 + 2 * u], b = acc[13 + 2 * u];
+      acc[12 + 2 * u] = a * cs + b * sn;
+      acc[13 + 2 * u] = b * cs - a * sn;
+    }
+  }
+  uint8_t* rec = out + row * 528;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    // Block 4 k + lane / 8: its eight lanes agree on the maximum.
+    float amax = fmaxf(fmaxf(fabsf(acc[4 * k]), fabsf(acc[4 * k + 1])), fmaxf(fabsf(acc[4 * k + 2]), fabsf(acc[4 * k + 3])));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+    const int e = fp8_block_exponent(amax);
+    const uint32_t word = e4m3x2(ldexpf(acc[4 * k], -e), ldexpf(acc[4 * k + 1], -e)) |
+                          (e4m3x2(ldexpf(acc[4 * k + 2], -e), ldexpf(acc[4 * k + 3], -e)) << 16);
+    *reinterpret_cast<uint32_t*>(rec + 128 * k + 4 * lane) = word;
+    if ((lane & 7) == 0) rec[512 + 4 * k + (lane >> 3)] = static_cast<uint8_t>(127 + e);
   }
   if (lane == 0) lse[row] = L;
 }
@@ -136,6 +200,26 @@ cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, con
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, d_num_splits, o_part, lse_part, out, lse, nq, h_q,
                             skip_single ? 1 : 0);
+}
+
+cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, const float* lse_part,
+                            const int32_t* positions, const RopeFreqs& freqs, uint8_t* out, float* lse, int nq,
+                            int h_q, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(nq) * h_q;
+  const int64_t blocks = (rows + kWarps - 1) / kWarps;
+  if (blocks == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rope_fp8_kernel, d_num_splits, o_part, lse_part, positions, freqs, out, lse, nq,
+                            h_q);
 }
 
 }  // namespace mla

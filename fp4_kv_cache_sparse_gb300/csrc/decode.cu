@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
       const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
       const int64_t split = static_cast<int64_t>(p.num_splits[qidx]) + local;
-      const bool direct = nsplit == 1;
+      const bool direct = nsplit == 1 && !p.force_partials;
       const bool split_ok = direct || (split >= 0 && split < p.ws_splits_cap && local < nsplit);
       if (i < NH) {
         const float l = red[i] + red[NH + i] + red[2 * NH + i] + red[3 * NH + i];

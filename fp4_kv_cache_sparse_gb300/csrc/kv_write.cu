@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 
 #include "../../include/mla.h"
+#include "mla_device.cuh"
 #include "mla_internal.h"
 
 namespace mla {
@@ -28,13 +29,6 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kRecFp8Bytes = 528;
 constexpr int kRecFp4Bytes = 288;
-
-// Two floats -> two E4M3FN bytes (lo in byte 0), nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 // Eight floats -> eight e2m1 nibbles (x[0] in the low nibble of byte 0).
 __device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8]) {
@@ -67,16 +61,6 @@ __device__ __forceinline__ void load16(const uint16_t* src, float (&x)[16]) {
     x[2 * k] = __uint_as_float(w[k] << 16);
     x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
   }
-}
-
-// Least e with amax * 2^-e <= 448 (0 for amax == 0), clamped to [-127, 127].
-__device__ __forceinline__ int fp8_block_exponent(float amax) {
-  if (!(amax > 0.f)) return 0;
-  int E;
-  frexpf(amax, &E);  // amax = f 2^E, f in [0.5, 1)
-  int e = E - 10;    // amax 2^-e >= 2^9 > 448
-  while (ldexpf(amax, -e) > 448.f) ++e;
-  return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
 __global__ void __launch_bounds__(kWarps * 32) kv_write_fp8_kernel(const uint16_t* __restrict__ lat,

@@ -315,4 +315,30 @@ __device__ __forceinline__ void dequant_fp4_16(uint32_t lo_word, uint32_t hi_wor
   }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 record encoding (the KV-cache writer and the FP8 output epilogue):
+// per 32-value block the least power of two 2^e with amax * 2^-e <= 448
+// (scale byte 127 + e; 0 for an all-zero block; e clamped to [-127, 127]),
+// each value x * 2^-e rounded to the nearest E4M3FN, ties to even,
+// saturating.  For fp32 inputs both steps are exact decisions: the scaling
+// is by a power of two and the conversion rounds the exact value once.
+// ---------------------------------------------------------------------------
+
+// Two floats -> two E4M3FN bytes (lo in byte 0), nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Least e with amax * 2^-e <= 448 (0 for amax == 0), clamped to [-127, 127].
+__device__ __forceinline__ int fp8_block_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int E;
+  frexpf(amax, &E);  // amax = f 2^E, f in [0.5, 1)
+  int e = E - 10;    // amax 2^-e >= 2^9 > 448
+  while (ldexpf(amax, -e) > 448.f) ++e;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
 }  // namespace mla

@@ -30,6 +30,7 @@ struct DecodeParams {
   int nq, h_q, n_hg, topk, xtopk, Tm, T;
   int64_t pool_tokens, xpool_tokens;
   float scale_log2;         // sm_scale * log2(e)
+  int force_partials;       // 1: every query token's result goes to the workspace (a later kernel finishes it)
 };
 
 // Work plan derived from the problem shape and the SM count.
@@ -63,6 +64,16 @@ cudaError_t launch_metadata(const Plan& plan, int nq, int32_t* d_sched, int32_t*
 
 cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, const float* lse_part, uint16_t* out,
                            float* lse, int nq, int h_q, bool skip_single, cudaStream_t stream);
+
+// Merge of each query token's split partials (every token, one split or
+// several), conjugate rotary embedding of dims 448..511 and the cast to
+// 528-byte FP8 records.  freqs[j] = theta^(-2j/64).
+struct RopeFreqs {
+  double f[32];
+};
+cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, const float* lse_part,
+                            const int32_t* positions, const RopeFreqs& freqs, uint8_t* out, float* lse, int nq,
+                            int h_q, cudaStream_t stream);
 
 cudaError_t launch_dequant(int kv_format, const uint8_t* records, int64_t n, uint16_t* out, cudaStream_t stream);
 

@@ -160,6 +160,40 @@ mla_status_t mla_sparse_decode(const mla_problem_t* problem,
                                mla_stream_t stream);
 
 /*
+ * The decode step with the fused output epilogue ("deepseek-ai/FlashMLA",
+ * "What it is": the conjugate RoPE on the output side and the final cast to
+ * FP8, outputs ready for a downstream FP8 einsum; "flops/attn-mla-kernel-
+ * support-matrix", "notes": qk_rope_head_dim = 64).  Same inputs and LSE as
+ * mla_sparse_decode; instead of the bf16 output, each (query token, head)
+ * row is
+ *   1. the attention output o (fp32, before any rounding),
+ *   2. turned on its rotary part -- dims 448..511 as 32 interleaved pairs
+ *      (448 + 2j, 449 + 2j) -- by the conjugate rotation: pair j by
+ *      -pos * rope_theta^(-2j/64), (a, b) -> (a cos + b sin, b cos - a sin),
+ *      pos = positions[b][s],
+ *   3. cast to a 528-byte FP8 record in the cache's own format (512 E4M3FN
+ *      bytes in dim order, then one e8m0 scale per 32 dims, the writer's
+ *      rule: the least power of two 2^e with block amax * 2^-e <= 448, each
+ *      value rounded to nearest even).
+ *   positions   int32 [batch][seq_len_q] (device): each query token's position.
+ *   rope_theta  the rotary base (> 1), e.g. 10000.
+ *   out_fp8     uint8 [batch][seq_len_q][h_q][528] (device, 4-byte aligned).
+ * The workspace must be at least what mla_get_metadata reports: every query
+ * token's result passes through it (one split or more) on its way to the
+ * epilogue, which runs in the merge kernel.  Rejections and errors as for
+ * mla_sparse_decode; a null positions or out_fp8, or a theta that is not
+ * finite and > 1, is MLA_ERR_INVALID_ARG.
+ */
+mla_status_t mla_sparse_decode_rope_fp8(const mla_problem_t* problem,
+                                        const void* q, const void* kv, const int32_t* indices,
+                                        const void* extra_kv, const int32_t* extra_indices,
+                                        const int32_t* d_sched, const int32_t* d_num_splits, int32_t num_parts,
+                                        void* workspace, size_t workspace_bytes,
+                                        const int32_t* positions, float rope_theta,
+                                        void* out_fp8, float* lse, int32_t* d_error,
+                                        mla_stream_t stream);
+
+/*
  * Merge of split-KV partial results ("Workarounds": split decoding with
  * num_splits).  For query token q its splits are
  * num_splits[q] .. num_splits[q+1]-1; split i of head h carries its own

@@ -174,3 +174,24 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         mla.dequantize(torch.zeros((4, 528), dtype=torch.uint8))
+
+
+def test_rope_fp8_decode_argument_checks_before_any_launch(lib):
+    """The fused-epilogue decode validates the problem first, then its own
+    arguments (positions, theta, the FP8 output), before any launch."""
+    p = _prob()
+    st, parts, ws = _query(lib, p)
+    A = ctypes.c_void_p(1 << 20)
+
+    def call(pos=A, theta=10000.0, out=A, prob=p, lse=A):
+        return lib.mla_sparse_decode_rope_fp8(ctypes.byref(prob), A, A, A, None, None, A, A, parts, A, ws, pos,
+                                              ctypes.c_float(theta), out, lse, None, None)
+
+    assert call(pos=None) == INVALID
+    assert call(pos=ctypes.c_void_p((1 << 20) + 2)) == INVALID
+    assert call(out=None) == INVALID
+    assert call(theta=1.0) == INVALID
+    assert call(theta=float("nan")) == INVALID
+    assert call(theta=float("inf")) == INVALID
+    assert call(lse=None) == INVALID
+    assert call(prob=_prob(h_q=48), pos=None) == UNSUPPORTED       # the problem is checked first
