@@ -1,5 +1,6 @@
 """GPU split merge (mla_combine) against the oracle's merge, and the
-scheduler metadata against a restatement of its partition rule."""
+scheduler metadata against the properties a schedule must have (checked
+from its own output, not against a copy of the rule that made it)."""
 import math
 
 import numpy as np
@@ -41,21 +42,35 @@ def test_combine_matches_oracle_merge():
     assert np.all(got[5] == 0) and np.all(np.isneginf(gl[5]))
 
 
-def _restated(p, num_sms):
-    nh = min(p.h_q, 64)
-    T = math.ceil(p.topk / 128) + math.ceil(p.extra_topk / 128)
-    nq = p.batch * p.seq_len_q
+def _check_schedule(sched, nsplit, parts, nq, T, max_parts):
+    """What "Tile-scheduler metadata" and "split decoding with num_splits"
+    ("flops/flashmla-decode-fp8-fp4-kv", "Workarounds") require of the
+    schedule, read off the schedule itself:
+      - the parts' item ranges [g0, g1) cover 0 .. nq*T once, in order;
+      - parts are balanced: every part but the last holds the same number
+        of items, the last no more, and there are no more parts than SMs per
+        head group;
+      - a query token's split count is the number of parts its items fall
+        into, and the prefix of those counts is num_splits;
+      - a part's first-split id is the number of earlier parts that hold
+        items of its first query token, and its first token is g0 // T."""
     G = nq * T
-    target = min(max(num_sms // (p.h_q // nh), 1), G)
-    S = math.ceil(G / target)
-    parts = math.ceil(G / S)
-    sched = []
+    assert 1 <= parts <= max(max_parts, 1)
+    g0, g1 = sched[:, 0].astype(np.int64), sched[:, 1].astype(np.int64)
+    assert g0[0] == 0 and g1[-1] == G
+    assert np.all(g1 > g0) and np.all(g0[1:] == g1[:-1])
+    size = g1 - g0
+    assert np.all(size[:-1] == size[0]) and size[-1] <= size[0]
+    counts = np.zeros(nq, dtype=np.int64)
+    first_local = []
     for k in range(parts):
-        g0, g1 = k * S, min(G, (k + 1) * S)
-        q0 = g0 // T
-        sched.append([g0, g1, k - (q0 * T) // S, q0, 0, 0, 0, 0])
-    splits = [((q + 1) * T - 1) // S - (q * T) // S + 1 for q in range(nq)]
-    return np.array(sched, np.int32), np.concatenate([[0], np.cumsum(splits)]).astype(np.int32)
+        qa, qb = g0[k] // T, (g1[k] - 1) // T
+        assert sched[k, 3] == qa
+        first_local.append(int(counts[qa]))
+        counts[qa:qb + 1] += 1
+    assert np.array_equal(sched[:, 2], np.array(first_local))
+    assert np.array_equal(nsplit, np.concatenate([[0], np.cumsum(counts)]))
+    assert np.all(sched[:, 4:] == 0)
 
 
 @pytest.mark.parametrize("shape", [
@@ -64,14 +79,15 @@ def _restated(p, num_sms):
     dict(batch=128, seq_len_q=2, h_q=128, topk=2048, num_pages=128 * 2048),
     dict(batch=32, seq_len_q=1, h_q=16, topk=65536, num_pages=32 * 16384),
     dict(batch=1500, seq_len_q=1, h_q=32, topk=300, num_pages=4),
+    dict(batch=64, seq_len_q=1, h_q=64, topk=2048, num_pages=64 * 1024, extra_topk=512, extra_num_pages=64 * 256),
 ])
 @pytest.mark.parametrize("num_sms", [0, 1, 152, 5000])
-def test_metadata_matches_partition_rule(shape, num_sms):
+def test_metadata_is_a_balanced_ordered_partition(shape, num_sms):
     p = mla.Problem.make(**shape)
     sched, nsplit, parts, _ = mla.get_metadata(p, num_sms)
     torch.cuda.synchronize()
     sms = num_sms or torch.cuda.get_device_properties(0).multi_processor_count
-    rs, rn = _restated(p, sms)
-    assert parts == rs.shape[0]
-    assert np.array_equal(sched.cpu().numpy(), rs)
-    assert np.array_equal(nsplit.cpu().numpy(), rn)
+    T = math.ceil(p.topk / 128) + math.ceil(p.extra_topk / 128)
+    head_groups = p.h_q // min(p.h_q, 64)
+    _check_schedule(sched.cpu().numpy().astype(np.int64), nsplit.cpu().numpy().astype(np.int64), parts,
+                    p.batch * p.seq_len_q, T, max(sms // head_groups, 1))
