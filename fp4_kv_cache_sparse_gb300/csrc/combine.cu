@@ -123,10 +123,11 @@ __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* 
 
 // The fused output epilogue ("deepseek-ai/FlashMLA", "What it is": the
 // conjugate RoPE on the output side and the cast to FP8).  Every query
-// token's splits (one or more) are merged as above; then dims 448..511 (the
+// token's splits (one or more; with skip_single only tokens of several
+// splits, the 128-head decode kernel having written the others with the
+// same arithmetic) are merged as above; then dims 448..511 (the
 // rotary part: 32 interleaved pairs, held by lanes 16..31 in acc[12..15])
-// turn by -phi_j, phi_j = pos * theta^(-2j/64), the angle taken in double
-// and reduced to [-pi, pi] before the float sine and cosine; then each
+// turn by -phi_j, phi_j = pos * theta^(-2j/64) (rope_conj_pair); then each
 // 32-dim block (eight lanes) is cast to E4M3FN under its e8m0 scale, giving
 // a 528-byte record per row in the cache's own format.
 __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t* __restrict__ num_splits,
@@ -134,7 +135,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t*
                                                               const float* __restrict__ lse_part,
                                                               const int32_t* __restrict__ positions,
                                                               const RopeFreqs freqs, uint8_t* __restrict__ out,
-                                                              float* __restrict__ lse, int nq, int h_q) {
+                                                              float* __restrict__ lse, int nq, int h_q,
+                                                              int skip_single) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
@@ -143,23 +145,14 @@ __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t*
   const int h = static_cast<int>(row % h_q);
   const int s0 = num_splits[qidx];
   const int n = num_splits[qidx + 1] - s0;
+  if (skip_single && n == 1) return;  // written by the decode kernel itself
   float acc[16];
   const float L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
   if (lane >= 16) {
     const double pos = static_cast<double>(positions[qidx]);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int j = 2 * (lane - 16) + u;  // pair (448 + 2j, 449 + 2j)
-      double phi = pos * freqs.f[j];
-      phi -= 6.283185307179586 * rint(phi * 0.15915494309189535);
-      // |phi| <= pi here, where the fast sine and cosine are within
-      // 2^-21 absolute: far below one E4M3 step of the result.
-      float sn, cs;
-      __sincosf(static_cast<float>(phi), &sn, &cs);
-      const float a = acc[12 + 2 * u], b = acc[13 + 2 * u];
-      acc[12 + 2 * u] = a * cs + b * sn;
-      acc[13 + 2 * u] = b * cs - a * sn;
-    }
+    for (int u = 0; u < 2; ++u)  // pair (448 + 2j, 449 + 2j), j = 2 (lane - 16) + u
+      rope_conj_pair(acc[12 + 2 * u], acc[13 + 2 * u], pos, freqs.f[2 * (lane - 16) + u]);
   }
   uint8_t* rec = out + row * 528;
 #pragma unroll
@@ -204,7 +197,7 @@ cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, con
 
 cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, const float* lse_part,
                             const int32_t* positions, const RopeFreqs& freqs, uint8_t* out, float* lse, int nq,
-                            int h_q, cudaStream_t stream) {
+                            int h_q, bool skip_single, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(nq) * h_q;
   const int64_t blocks = (rows + kWarps - 1) / kWarps;
   if (blocks == 0) return cudaSuccess;
@@ -219,7 +212,7 @@ cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, co
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, rope_fp8_kernel, d_num_splits, o_part, lse_part, positions, freqs, out, lse, nq,
-                            h_q);
+                            h_q, skip_single ? 1 : 0);
 }
 
 }  // namespace mla

@@ -168,18 +168,7 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M rows (lanes) x K
-// columns of packed bf16 pairs.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// One elected lane of a converged warp issues (same products as above).
+// columns of packed bf16 pairs.  One elected lane of a converged warp issues.
 __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
   asm volatile(
@@ -271,6 +260,10 @@ __device__ __forceinline__ PSpan pair_span(const DecodeParams& p, int part) {
   return s;
 }
 
+// kRope: query tokens of one split leave as FP8 records after the
+// conjugate rotary embedding (the fused epilogue) instead of bf16 rows; a
+// separate instantiation, so that the bf16 kernel carries none of it.
+template <bool kRope>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kv_map) {
   using L = PairSmem;
@@ -659,6 +652,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // Likewise the O rows out: 32-byte stores when the destination allows.
     const bool out_al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
     const bool ws_al32 = (reinterpret_cast<uintptr_t>(p.ws_o) & 31) == 0;
+    // FP8 records (528 bytes, a multiple of 16) in 16-byte pieces when the
+    // destination allows, else in 4-byte words.
+    const bool rope_al16 = (reinterpret_cast<uintptr_t>(p.rope_out) & 15) == 0;
     auto load_q = [&](int qx) {
       const uint4* src = q_src(qx);
 #pragma unroll 1
@@ -934,11 +930,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       // out as whole row pieces: 64 bytes of one bf16 row or 128 bytes of
       // one fp32 row per group of lanes (32 bytes per lane when aligned).
       uint8_t* ost = sP + warp * 4096;
+      // The fused epilogue's records: this lane's head row, bytes d0 .. d0+31
+      // and scale byte 512 + d0 / 32 for each 32-dim block d0 of this warp.
+      const bool rope = kRope && direct;
+      uint8_t* rec = rope ? p.rope_out + (static_cast<int64_t>(qidx) * p.h_q + i) * 528 : nullptr;
+      uint32_t sbytes = 0;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t o[32];
         tmem_ld32(tO + 128 * ch + 32 * j, o);
         const int d0 = static_cast<int>(c) * kHalf + 128 * ch + 32 * j;
+        if constexpr (kRope) {
+          if (rope) {
+            // O / l, the conjugate rotation of dims 448..511 (pairs
+            // (448 + 2m, 449 + 2m)), then E4M3FN under the block's e8m0 scale:
+            // the arithmetic of the merge kernel's fused epilogue.
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * linv;
+            if (d0 >= 448) {
+              const double pos = static_cast<double>(p.positions[qidx]);
+              const double* f = p.rope.f + (d0 - 448) / 2;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) rope_conj_pair(v[2 * e], v[2 * e + 1], pos, f[e]);
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+            const int ex = fp8_block_exponent(amax);
+            uint32_t w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              w[u] = e4m3x2(ldexpf(v[4 * u], -ex), ldexpf(v[4 * u + 1], -ex)) |
+                     (e4m3x2(ldexpf(v[4 * u + 2], -ex), ldexpf(v[4 * u + 3], -ex)) << 16);
+            if (rope_al16) {
+              *reinterpret_cast<uint4*>(rec + d0) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4*>(rec + d0 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) *reinterpret_cast<uint32_t*>(rec + d0 + 4 * u) = w[u];
+            }
+            sbytes |= static_cast<uint32_t>(127 + ex) << (8 * j);
+            __syncwarp();
+            continue;
+          }
+        }
         if (direct) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -991,6 +1027,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
         __syncwarp();  // this warp's staging block is rewritten next
       }
+      if constexpr (kRope) {
+        if (rope) *reinterpret_cast<uint32_t*>(rec + 512 + 8 * static_cast<int>(c) + 4 * ch) = sbytes;
+      }
       // No warp sends the next partial scores (after which the peer's next P
       // lands here) or writes the next P before every warp's O rows have
       // been read out of the P buffers.
@@ -1017,8 +1056,12 @@ int decode_pair_smem_bytes() { return PairSmem::kAlloc; }
 
 cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_t stream) {
   constexpr int smem = PairSmem::kAlloc;
-  static std::atomic<uint64_t> configured{0};
-  cudaError_t e0 = max_dynamic_smem_once(configured, reinterpret_cast<const void*>(sparse_decode_pair_kernel), smem);
+  const bool rope = p.rope_out != nullptr;
+  static std::atomic<uint64_t> configured{0}, configured_rope{0};
+  cudaError_t e0 = rope ? max_dynamic_smem_once(configured_rope,
+                                                reinterpret_cast<const void*>(sparse_decode_pair_kernel<true>), smem)
+                        : max_dynamic_smem_once(configured,
+                                                reinterpret_cast<const void*>(sparse_decode_pair_kernel<false>), smem);
   if (e0 != cudaSuccess) return e0;
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -1034,7 +1077,10 @@ cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  sparse_decode_pair_kernel<<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map);
+  if (rope)
+    sparse_decode_pair_kernel<true><<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map);
+  else
+    sparse_decode_pair_kernel<false><<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map);
   return cudaGetLastError();
 }
 

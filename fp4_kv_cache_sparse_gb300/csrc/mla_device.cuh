@@ -332,6 +332,22 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 }
 
 // Least e with amax * 2^-e <= 448 (0 for amax == 0), clamped to [-127, 127].
+// Conjugate rotary embedding of one interleaved pair (a, b) by
+// phi = pos * freq ("deepseek-ai/FlashMLA", "What it is": the output-side
+// RoPE): the angle is taken in double and reduced to [-pi, pi], where the
+// fast float sine and cosine are within 2^-21 absolute (far below one E4M3
+// step of the result); (a, b) -> (a cos + b sin, b cos - a sin), rounded in
+// one fixed order so that every kernel using it gives the same bytes.
+__device__ __forceinline__ void rope_conj_pair(float& a, float& b, double pos, double freq) {
+  double phi = pos * freq;
+  phi -= 6.283185307179586 * rint(phi * 0.15915494309189535);
+  float sn, cs;
+  __sincosf(static_cast<float>(phi), &sn, &cs);
+  const float x = a, y = b;
+  a = __fmaf_rn(x, cs, __fmul_rn(y, sn));
+  b = __fmaf_rn(y, cs, -__fmul_rn(x, sn));
+}
+
 __device__ __forceinline__ int fp8_block_exponent(float amax) {
   if (!(amax > 0.f)) return 0;
   int E;

@@ -13,6 +13,12 @@
 namespace mla {
 
 // Everything the decode kernel reads, resolved by the host layer.
+// Output-side rotary frequencies of the fused epilogue: freqs[j] =
+// theta^(-2j/64) for the pair (448 + 2j, 449 + 2j).
+struct RopeFreqs {
+  double f[32];
+};
+
 struct DecodeParams {
   const uint16_t* q;        // bf16 [nq][h_q][512]
   const uint8_t* kv;        // FP8 records
@@ -31,6 +37,12 @@ struct DecodeParams {
   int64_t pool_tokens, xpool_tokens;
   float scale_log2;         // sm_scale * log2(e)
   int force_partials;       // 1: every query token's result goes to the workspace (a later kernel finishes it)
+  // Fused output epilogue written by the decode kernel itself for query
+  // tokens of one split (128-head kernel only): null, or [nq][h_q][528]
+  // FP8 records after the conjugate rotary embedding at positions[qidx].
+  uint8_t* rope_out;
+  const int32_t* positions;
+  RopeFreqs rope;
 };
 
 // Work plan derived from the problem shape and the SM count.
@@ -65,15 +77,12 @@ cudaError_t launch_metadata(const Plan& plan, int nq, int32_t* d_sched, int32_t*
 cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, const float* lse_part, uint16_t* out,
                            float* lse, int nq, int h_q, bool skip_single, cudaStream_t stream);
 
-// Merge of each query token's split partials (every token, one split or
-// several), conjugate rotary embedding of dims 448..511 and the cast to
-// 528-byte FP8 records.  freqs[j] = theta^(-2j/64).
-struct RopeFreqs {
-  double f[32];
-};
+// Merge of each query token's split partials (with skip_single, only tokens
+// of more than one split), conjugate rotary embedding of dims 448..511 and
+// the cast to 528-byte FP8 records.
 cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, const float* lse_part,
                             const int32_t* positions, const RopeFreqs& freqs, uint8_t* out, float* lse, int nq,
-                            int h_q, cudaStream_t stream);
+                            int h_q, bool skip_single, cudaStream_t stream);
 
 cudaError_t launch_dequant(int kv_format, const uint8_t* records, int64_t n, uint16_t* out, cudaStream_t stream);
 

@@ -178,9 +178,12 @@ mla_status_t mla_sparse_decode(const mla_problem_t* problem,
  *   positions   int32 [batch][seq_len_q] (device): each query token's position.
  *   rope_theta  the rotary base (> 1), e.g. 10000.
  *   out_fp8     uint8 [batch][seq_len_q][h_q][528] (device, 4-byte aligned).
- * The workspace must be at least what mla_get_metadata reports: every query
- * token's result passes through it (one split or more) on its way to the
- * epilogue, which runs in the merge kernel.  Rejections and errors as for
+ * The workspace must be at least what mla_get_metadata reports.  With 128
+ * heads and no extra cache, the decode kernel writes the records of query
+ * tokens that have one split itself and only tokens of several splits pass
+ * through the workspace to the merge kernel (the same arithmetic either
+ * way); for other shapes every query token's result passes through it on
+ * its way to the epilogue in the merge kernel.  Rejections and errors as for
  * mla_sparse_decode; a null positions or out_fp8, or a theta that is not
  * finite and > 1, is MLA_ERR_INVALID_ARG.
  */

@@ -86,24 +86,29 @@ def test_rope_fp8_matches_the_oracle(cid, batch):
     _run(w, all_queries(w), positions)
 
 
+@pytest.mark.parametrize("cid", [1, 2])
 @pytest.mark.parametrize("num_sms", [1, 20, 100000])
-def test_rope_fp8_with_any_split_count(num_sms):
+def test_rope_fp8_with_any_split_count(cid, num_sms):
     """One part, parts that end one token's split and start the next's,
     one tile per part: every query token's splits are merged before the
-    rotation and the cast."""
-    w = synth.make_workload(1, batch=3, workers=1)
-    positions = np.array([[5], [4096], [131071]])
+    rotation and the cast.  At 128 heads a query token of one split is
+    written by the decode kernel itself (every token with one part, none
+    with one tile per part)."""
+    w = synth.make_workload(cid, batch=3, workers=1)
+    positions = (np.array([5, 4096, 131071])[:, None] + 977 * np.arange(w.cfg.seq_len_q)[None, :]) % (1 << 17)
     _run(w, all_queries(w), positions, num_sms=num_sms)
 
 
-def test_rope_fp8_position_zero_and_empty_rows():
+@pytest.mark.parametrize("cid", [1, 2])
+def test_rope_fp8_position_zero_and_empty_rows(cid):
     """Position 0 turns nothing (the records are the plain FP8 cast of the
     output); a query token with no valid index gives all-zero codes under
-    scale byte 127 and -inf."""
-    w = synth.make_workload(1, batch=2, workers=1)
+    scale byte 127 and -inf (64 heads through the merge, 128 heads from
+    the decode kernel's own epilogue with one part)."""
+    w = synth.make_workload(cid, batch=2, workers=1)
     w.idx[1] = -1
-    positions = np.zeros((2, 1), dtype=np.int64)
-    out, lse = _run(w, all_queries(w), positions)
+    positions = np.zeros((2, w.cfg.seq_len_q), dtype=np.int64)
+    out, lse = _run(w, all_queries(w), positions, num_sms=1)
     rec = out[1].cpu().numpy().reshape(-1, 528)
     assert np.all(rec[:, :512] == 0) and np.all(rec[:, 512:] == 127)
     assert torch.isneginf(lse[1]).all()
