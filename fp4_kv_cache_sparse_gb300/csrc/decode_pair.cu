@@ -299,17 +299,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bars[bSclFull + i], 1);
       mbar_init(&bars[bSclFree + i], kProdWarps);
       mbar_init(&bars[bMaskFull + i], 1);
-      mbar_init(&bars[bMaskFree + i], kSoftThreads);
+      mbar_init(&bars[bMaskFree + i], kSoftThreads / 32);  // per-warp arrivals (lane 0 after __syncwarp)
       mbar_init(&bars[bStatsIn + i], 1);
       mbar_init(&bars[bSFull + i], 1);
-      mbar_init(&bars[bSUsed + i], kSoftThreads);
+      mbar_init(&bars[bSUsed + i], kSoftThreads / 32);
     }
     for (int b = 0; b < kKvBufs; ++b) {
       mbar_init(&bars[bKvFull + b], 2 * kProdWarps);  // two 32-token slots per 64-token sub-tile
       mbar_init(&bars[bKvFree + b], 1);
     }
-    mbar_init(&bars[bQFull], kSoftThreads);
-    for (int b = 0; b < 2; ++b) mbar_init(&bars[bPMine2 + b], kSoftThreads);
+    mbar_init(&bars[bQFull], kSoftThreads / 32);  // one arrival per softmax warp, after its lanes' writes
+    for (int b = 0; b < 2; ++b) mbar_init(&bars[bPMine2 + b], kSoftThreads / 32);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[bPIn + b], 1);
       mbar_init(&bars[bPvDone + b], 1);
@@ -677,7 +677,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars[bQFull]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bQFull]);
     };
     if (span.g_begin < span.g_end) load_q(static_cast<int>(span.g_begin / p.T));
     for (int64_t g = span.g_begin; g < span.g_end;) {
@@ -699,7 +700,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         uint32_t mkw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) mkw[e] = sMask[mp * 4 + e];
-        mbar_arrive(&bars[bMaskFree + mp]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[bMaskFree + mp]);
 #pragma unroll 1
         for (int sub = 0; sub < 2; ++sub, ++n_sub) {
           const uint32_t sb = n_sub & 1, pb = n_sub & 1;  // S, P and X buffers of this sub-tile
@@ -845,7 +847,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           }
           // S of this sub-tile has been read for the last time.
           tc_fence_before();
-          mbar_arrive(&bars[bSUsed + sb]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[bSUsed + sb]);
           // alpha == 0 only while m was -inf: O then holds zeros (every P so
           // far was 0) or, on a segment's first sub-tile, values that this
           // sub-tile's PV overwrites; either way nothing needs scaling.
@@ -867,7 +870,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           //    of the next sub-tile covers the copy's reads.
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(&bars[bPMine2 + pb]);  // the tensor core may start on this CTA's tokens
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[bPMine2 + pb]);  // the tensor core may start on this CTA's tokens
           __syncwarp();
           if (lane == 0) {
             // The peer's block for these rows is free: the peer's warps
