@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* 
 // splits, the 128-head decode kernel having written the others with the
 // same arithmetic) are merged as above; then dims 448..511 (the
 // rotary part: 32 interleaved pairs, held by lanes 16..31 in acc[12..15])
-// turn by -phi_j, phi_j = pos * theta^(-2j/64) (rope_conj_pair); then each
+// turn by -phi_j, phi_j = pos * theta^(-2j/64) (rope_cos_sin, rope_conj_apply); then each
 // 32-dim block (eight lanes) is cast to E4M3FN under its e8m0 scale, giving
 // a 528-byte record per row in the cache's own format.
 __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t* __restrict__ num_splits,
@@ -151,8 +151,11 @@ __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t*
   if (lane >= 16) {
     const double pos = static_cast<double>(positions[qidx]);
 #pragma unroll
-    for (int u = 0; u < 2; ++u)  // pair (448 + 2j, 449 + 2j), j = 2 (lane - 16) + u
-      rope_conj_pair(acc[12 + 2 * u], acc[13 + 2 * u], pos, freqs.f[2 * (lane - 16) + u]);
+    for (int u = 0; u < 2; ++u) {  // pair (448 + 2j, 449 + 2j), j = 2 (lane - 16) + u
+      float cs, sn;
+      rope_cos_sin(pos, freqs.f[2 * (lane - 16) + u], cs, sn);
+      rope_conj_apply(acc[12 + 2 * u], acc[13 + 2 * u], cs, sn);
+    }
   }
   uint8_t* rec = out + row * 528;
 #pragma unroll

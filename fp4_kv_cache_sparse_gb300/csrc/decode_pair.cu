@@ -939,6 +939,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const bool rope = kRope && direct;
       uint8_t* rec = rope ? p.rope_out + (static_cast<int64_t>(qidx) * p.h_q + i) * 528 : nullptr;
       uint32_t sbytes = 0;
+      // The warps holding dims 448..511 take pair m's angle once, in lane m,
+      // for all 32 rows (it depends on the position and m only).
+      float rope_cs = 1.f, rope_sn = 0.f;
+      if (rope && static_cast<int>(c) * kHalf + 128 * ch + 96 >= 448)
+        rope_cos_sin(static_cast<double>(p.positions[qidx]), p.rope.f[lane], rope_cs, rope_sn);
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         uint32_t o[32];
@@ -953,10 +958,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * linv;
             if (d0 >= 448) {
-              const double pos = static_cast<double>(p.positions[qidx]);
-              const double* f = p.rope.f + (d0 - 448) / 2;
 #pragma unroll
-              for (int e = 0; e < 16; ++e) rope_conj_pair(v[2 * e], v[2 * e + 1], pos, f[e]);
+              for (int e = 0; e < 16; ++e) {
+                const int m = (d0 - 448) / 2 + e;  // lane m holds pair m's angle
+                rope_conj_apply(v[2 * e], v[2 * e + 1], __shfl_sync(0xFFFFFFFFu, rope_cs, m),
+                                __shfl_sync(0xFFFFFFFFu, rope_sn, m));
+              }
             }
             float amax = 0.f;
 #pragma unroll

@@ -334,15 +334,19 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // Least e with amax * 2^-e <= 448 (0 for amax == 0), clamped to [-127, 127].
 // Conjugate rotary embedding of one interleaved pair (a, b) by
 // phi = pos * freq ("deepseek-ai/FlashMLA", "What it is": the output-side
-// RoPE): the angle is taken in double and reduced to [-pi, pi], where the
-// fast float sine and cosine are within 2^-21 absolute (far below one E4M3
-// step of the result); (a, b) -> (a cos + b sin, b cos - a sin), rounded in
-// one fixed order so that every kernel using it gives the same bytes.
-__device__ __forceinline__ void rope_conj_pair(float& a, float& b, double pos, double freq) {
+// RoPE), in two steps so that a kernel can compute each pair's angle once
+// and apply it to many rows: rope_cos_sin takes the angle in double,
+// reduces it to [-pi, pi] (where the fast float sine and cosine are within
+// 2^-21 absolute, far below one E4M3 step of the result) and returns its
+// float cosine and sine; rope_conj_apply maps (a, b) -> (a cos + b sin,
+// b cos - a sin), rounded in one fixed order so that every kernel using the
+// pair of routines gives the same bytes.
+__device__ __forceinline__ void rope_cos_sin(double pos, double freq, float& cs, float& sn) {
   double phi = pos * freq;
   phi -= 6.283185307179586 * rint(phi * 0.15915494309189535);
-  float sn, cs;
   __sincosf(static_cast<float>(phi), &sn, &cs);
+}
+__device__ __forceinline__ void rope_conj_apply(float& a, float& b, float cs, float sn) {
   const float x = a, y = b;
   a = __fmaf_rn(x, cs, __fmul_rn(y, sn));
   b = __fmaf_rn(y, cs, -__fmul_rn(x, sn));
