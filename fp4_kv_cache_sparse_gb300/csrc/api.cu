@@ -243,10 +243,13 @@ mla_status_t mla_sparse_decode(const mla_problem_t* problem, const void* q, cons
                      workspace_bytes, static_cast<uint16_t*>(out), lse, d_error, false, nullptr, stream, &p);
   if (st != MLA_OK) return st;
   if (num_parts > 1) {
-    // Only query tokens with more than one split have partials to merge;
-    // the kernel skips the others.
-    if (launch_combine(d_num_splits, p.ws_o, p.ws_lse, p.out, lse, p.nq, problem->h_q, true,
-                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // Only query tokens with more than one split have partials to merge: a
+    // grid over parts visits just those (at most one per part) and is the
+    // smaller grid when parts are fewer than query tokens; otherwise one warp
+    // per row, the kernel skipping one-split rows.
+    const int32_t* by_part = num_parts < p.nq ? d_sched : nullptr;
+    if (launch_combine(d_num_splits, p.ws_o, p.ws_lse, p.out, lse, p.nq, problem->h_q, true, by_part, num_parts,
+                       p.T, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
   return MLA_OK;
@@ -276,6 +279,7 @@ mla_status_t mla_sparse_decode_rope_fp8(const mla_problem_t* problem, const void
                      workspace_bytes, nullptr, lse, d_error, !direct, direct ? &ro : nullptr, stream, &p);
   if (st != MLA_OK) return st;
   if (launch_rope_fp8(d_num_splits, p.ws_o, p.ws_lse, positions, ro.freqs, ro.out, lse, p.nq, problem->h_q, direct,
+                      direct && num_parts < p.nq ? d_sched : nullptr, num_parts, p.T,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
@@ -292,7 +296,7 @@ mla_status_t mla_combine(const mla_problem_t* problem, const int32_t* d_num_spli
     return MLA_ERR_INVALID_ARG;
   const int nq = problem->batch * problem->seq_len_q;
   if (launch_combine(d_num_splits, o_partial, lse_partial, static_cast<uint16_t*>(out), lse, nq, problem->h_q,
-                     false, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                     false, nullptr, 0, 0, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -89,20 +89,45 @@ __device__ __forceinline__ float merge_row(const float* __restrict__ o_part, con
   return L;
 }
 
+// The query token and head of this warp.  kByPart: blockIdx.x is a part of
+// the decode's schedule and blockIdx.y a group of kWarps heads; the only
+// query token of a part that can have several splits is the one holding the
+// part's last tile, and it is merged by the part in which it starts (so
+// once); -1 when the part has nothing to merge.  Otherwise one warp per
+// (query token, head) row, every token visited.
+template <bool kByPart>
+__device__ __forceinline__ int64_t merge_row_of(const int32_t* __restrict__ sched, int T, int h_q, int& h) {
+  const int warp = threadIdx.x >> 5;
+  if constexpr (!kByPart) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    h = static_cast<int>(row % h_q);
+    return row / h_q;
+  }
+  const int32_t* e = sched + static_cast<int64_t>(blockIdx.x) * MLA_SCHED_INTS;
+  const int64_t g0 = e[0], g1 = e[1];
+  h = static_cast<int>(blockIdx.y) * kWarps + warp;
+  if (g1 <= g0 || T <= 0) return -1;
+  const int64_t q = (g1 - 1) / T;
+  return q * T >= g0 ? q : -1;
+}
+
+template <bool kByPart>
 __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* __restrict__ num_splits,
                                                              const float* __restrict__ o_part,
                                                              const float* __restrict__ lse_part,
                                                              uint16_t* __restrict__ out, float* __restrict__ lse,
-                                                             int nq, int h_q, int skip_single) {
+                                                             int nq, int h_q, int skip_single,
+                                                             const int32_t* __restrict__ sched, int T) {
   // Launched as a programmatic dependent of the decode kernel: wait until
   // that grid has completed and its partials are visible (returns at once
   // for an ordinary launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (row >= static_cast<int64_t>(nq) * h_q) return;  // whole warps leave together
-  const int qidx = static_cast<int>(row / h_q);
-  const int h = static_cast<int>(row % h_q);
+  int h;
+  const int64_t q = merge_row_of<kByPart>(sched, T, h_q, h);
+  if (q < 0 || q >= nq || h >= h_q) return;  // whole warps leave together
+  const int qidx = static_cast<int>(q);
+  const int64_t row = q * h_q + h;
   const int s0 = num_splits[qidx];
   const int n = num_splits[qidx + 1] - s0;
   if (skip_single && n == 1) return;
@@ -130,19 +155,22 @@ __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* 
 // turn by -phi_j, phi_j = pos * theta^(-2j/64) (rope_cos_sin, rope_conj_apply); then each
 // 32-dim block (eight lanes) is cast to E4M3FN under its e8m0 scale, giving
 // a 528-byte record per row in the cache's own format.
+template <bool kByPart>
 __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t* __restrict__ num_splits,
                                                               const float* __restrict__ o_part,
                                                               const float* __restrict__ lse_part,
                                                               const int32_t* __restrict__ positions,
                                                               const RopeFreqs freqs, uint8_t* __restrict__ out,
                                                               float* __restrict__ lse, int nq, int h_q,
-                                                              int skip_single) {
+                                                              int skip_single, const int32_t* __restrict__ sched,
+                                                              int T) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (row >= static_cast<int64_t>(nq) * h_q) return;  // whole warps leave together
-  const int qidx = static_cast<int>(row / h_q);
-  const int h = static_cast<int>(row % h_q);
+  int h;
+  const int64_t q = merge_row_of<kByPart>(sched, T, h_q, h);
+  if (q < 0 || q >= nq || h >= h_q) return;  // whole warps leave together
+  const int qidx = static_cast<int>(q);
+  const int64_t row = q * h_q + h;
   const int s0 = num_splits[qidx];
   const int n = num_splits[qidx + 1] - s0;
   if (skip_single && n == 1) return;  // written by the decode kernel itself
@@ -176,16 +204,26 @@ __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t*
 
 }  // namespace
 
+// One warp per row (sched == null), or parts x head groups (only the rows of
+// split query tokens; the caller guarantees that every other row was written
+// by the decode kernel itself).
+static void merge_grid(int64_t rows, const int32_t* sched, int num_parts, int h_q, dim3& grid) {
+  if (sched != nullptr)
+    grid = dim3(static_cast<unsigned>(num_parts), static_cast<unsigned>((h_q + kWarps - 1) / kWarps));
+  else
+    grid = dim3(static_cast<unsigned>((rows + kWarps - 1) / kWarps));
+}
+
 cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, const float* lse_part, uint16_t* out,
-                           float* lse, int nq, int h_q, bool skip_single, cudaStream_t stream) {
+                           float* lse, int nq, int h_q, bool skip_single, const int32_t* sched, int num_parts, int T,
+                           cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(nq) * h_q;
-  const int64_t blocks = (rows + kWarps - 1) / kWarps;
-  if (blocks == 0) return cudaSuccess;
+  if (rows == 0 || (sched != nullptr && num_parts <= 0)) return cudaSuccess;
   // Programmatic stream serialization: the merge's blocks may be scheduled
   // while the preceding kernel drains; each waits for it (griddepcontrol)
   // before reading anything.
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  merge_grid(rows, sched, num_parts, h_q, cfg.gridDim);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -194,18 +232,21 @@ cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, d_num_splits, o_part, lse_part, out, lse, nq, h_q,
-                            skip_single ? 1 : 0);
+  if (sched != nullptr)
+    return cudaLaunchKernelEx(&cfg, combine_kernel<true>, d_num_splits, o_part, lse_part, out, lse, nq, h_q,
+                              skip_single ? 1 : 0, sched, T);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<false>, d_num_splits, o_part, lse_part, out, lse, nq, h_q,
+                            skip_single ? 1 : 0, sched, T);
 }
 
 cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, const float* lse_part,
                             const int32_t* positions, const RopeFreqs& freqs, uint8_t* out, float* lse, int nq,
-                            int h_q, bool skip_single, cudaStream_t stream) {
+                            int h_q, bool skip_single, const int32_t* sched, int num_parts, int T,
+                            cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(nq) * h_q;
-  const int64_t blocks = (rows + kWarps - 1) / kWarps;
-  if (blocks == 0) return cudaSuccess;
+  if (rows == 0 || (sched != nullptr && num_parts <= 0)) return cudaSuccess;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  merge_grid(rows, sched, num_parts, h_q, cfg.gridDim);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -214,8 +255,11 @@ cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, rope_fp8_kernel, d_num_splits, o_part, lse_part, positions, freqs, out, lse, nq,
-                            h_q, skip_single ? 1 : 0);
+  if (sched != nullptr)
+    return cudaLaunchKernelEx(&cfg, rope_fp8_kernel<true>, d_num_splits, o_part, lse_part, positions, freqs, out,
+                              lse, nq, h_q, skip_single ? 1 : 0, sched, T);
+  return cudaLaunchKernelEx(&cfg, rope_fp8_kernel<false>, d_num_splits, o_part, lse_part, positions, freqs, out, lse,
+                            nq, h_q, skip_single ? 1 : 0, sched, T);
 }
 
 }  // namespace mla

@@ -74,15 +74,21 @@ int decode_pair_smem_bytes();
 
 cudaError_t launch_metadata(const Plan& plan, int nq, int32_t* d_sched, int32_t* d_num_splits, cudaStream_t stream);
 
+// Merge of split partials.  With sched (the decode's part schedule, T
+// tiles per query token) only the rows of query tokens that have several
+// splits are visited, every other row having been written by the decode
+// kernel; without it every row is (skip_single then skips one-split rows).
 cudaError_t launch_combine(const int32_t* d_num_splits, const float* o_part, const float* lse_part, uint16_t* out,
-                           float* lse, int nq, int h_q, bool skip_single, cudaStream_t stream);
+                           float* lse, int nq, int h_q, bool skip_single, const int32_t* sched, int num_parts, int T,
+                           cudaStream_t stream);
 
 // Merge of each query token's split partials (with skip_single, only tokens
 // of more than one split), conjugate rotary embedding of dims 448..511 and
 // the cast to 528-byte FP8 records.
 cudaError_t launch_rope_fp8(const int32_t* d_num_splits, const float* o_part, const float* lse_part,
                             const int32_t* positions, const RopeFreqs& freqs, uint8_t* out, float* lse, int nq,
-                            int h_q, bool skip_single, cudaStream_t stream);
+                            int h_q, bool skip_single, const int32_t* sched, int num_parts, int T,
+                            cudaStream_t stream);
 
 cudaError_t launch_dequant(int kv_format, const uint8_t* records, int64_t n, uint16_t* out, cudaStream_t stream);
 
