@@ -204,6 +204,21 @@ def test_split_counts_do_not_change_results(num_sms, cid):
     compare(out, lse, w, all_queries(w))
 
 
+@pytest.mark.parametrize("cid,batch,num_sms", [(1, 16, 6), (2, 8, 12)])
+def test_merge_over_parts(cid, batch, num_sms):
+    """Fewer parts than query tokens (6 parts, 16 query tokens of 16 tiles):
+    the merge then runs over the parts and visits only the query tokens that
+    a part boundary splits; every other token must come out of the decode
+    kernel itself.  64 heads and 128 heads."""
+    w = synth.make_workload(cid, batch=batch, workers=1)
+    dw = DeviceWorkload(w)
+    dec = dw.decoder(num_sms)
+    assert 1 < dec.num_parts < w.cfg.batch * w.cfg.seq_len_q
+    out, lse, err = dw.run(dec=dec)
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
 def test_deterministic():
     w = synth.make_workload(2, batch=2, workers=1)
     dw = DeviceWorkload(w)

@@ -99,6 +99,15 @@ def test_rope_fp8_with_any_split_count(cid, num_sms):
     _run(w, all_queries(w), positions, num_sms=num_sms)
 
 
+def test_rope_fp8_merge_over_parts():
+    """128 heads, fewer parts than query tokens: one-split tokens written by
+    the decode kernel, the split ones by the merge over parts."""
+    w = synth.make_workload(2, batch=8, workers=1)
+    rng = np.random.default_rng(8)
+    positions = rng.integers(0, 1 << 17, size=(w.cfg.batch, w.cfg.seq_len_q))
+    _run(w, all_queries(w), positions, num_sms=12)
+
+
 @pytest.mark.parametrize("cid", [1, 2])
 def test_rope_fp8_position_zero_and_empty_rows(cid):
     """Position 0 turns nothing (the records are the plain FP8 cast of the
