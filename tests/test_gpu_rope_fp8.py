@@ -108,6 +108,32 @@ def test_rope_fp8_merge_over_parts():
     _run(w, all_queries(w), positions, num_sms=12)
 
 
+def test_rope_fp8_unaligned_records_match_aligned():
+    """Records written to a 4-byte (not 16-byte) aligned buffer -- word
+    stores in the 128-head kernel's own epilogue, the merge unchanged -- are
+    byte-identical to the aligned run, for one part (every token written by
+    the decode kernel) and for the default split."""
+    w = synth.make_workload(2, batch=2, workers=1)
+    dw = DeviceWorkload(w)
+    rng = np.random.default_rng(5)
+    pos = torch.from_numpy(rng.integers(0, 1 << 17, size=(w.cfg.batch, w.cfg.seq_len_q)).astype(np.int32)).to(dw.dev)
+    shape = (w.cfg.batch, w.cfg.seq_len_q, w.cfg.h_q, 528)
+    n = int(np.prod(shape))
+    for num_sms in (1, 0):
+        dec = dw.decoder(num_sms)
+        dec.error.zero_()
+        ref, ref_lse = dec.rope_fp8(dw.q, dw.kv, dw.idx, pos, THETA)
+        raw = torch.zeros((n + 16,), dtype=torch.uint8, device=dw.dev)
+        off = raw[4:4 + n].view(shape)
+        assert off.data_ptr() % 16 == 4
+        out, lse = dec.rope_fp8(dw.q, dw.kv, dw.idx, pos, THETA, out=off)
+        torch.cuda.synchronize()
+        assert int(dec.error.item()) == 0
+        assert torch.equal(out.cpu(), ref.cpu())
+        assert torch.equal(lse.cpu(), ref_lse.cpu())
+        assert int(raw[:4].sum()) == 0 and int(raw[4 + n:].sum()) == 0  # nothing written outside
+
+
 @pytest.mark.parametrize("cid", [1, 2])
 def test_rope_fp8_position_zero_and_empty_rows(cid):
     """Position 0 turns nothing (the records are the plain FP8 cast of the
