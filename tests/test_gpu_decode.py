@@ -35,14 +35,20 @@ def test_reduced_configs_all_queries(cid):
 @pytest.mark.parametrize("cid", [1, 2, 3, 4, 5, 6])
 def test_full_size_sampled_queries(cid):
     """The full workload in the launch configuration the benchmark times;
-    sampled query tokens against the oracle, the rest checked for finiteness
-    and the -inf/0 convention."""
+    sampled query tokens against the oracle (random ones plus the first two
+    that the schedule splits over parts, so that the merge is checked at full
+    size), the rest checked for finiteness and the -inf/0 convention."""
     w = synth.make_workload(cid)
     dw = DeviceWorkload(w)
-    out, lse, err = dw.run()
+    dec = dw.decoder()
+    out, lse, err = dw.run(dec=dec)
     assert err == 0
     assert torch.isfinite(out).all() and torch.isfinite(lse).all()
-    compare(out, lse, w, sample_queries(w, n=3, seed=cid))
+    qs = all_queries(w)
+    splits = np.diff(dec.num_splits.cpu().numpy())
+    split_q = [qs[j] for j in np.nonzero(splits > 1)[0][:2]]
+    picked = sorted(set(sample_queries(w, n=3, seed=cid)) | set(split_q))
+    compare(out, lse, w, picked)
 
 
 def test_scattered_skips():
