@@ -121,12 +121,16 @@ def test_all_skipped_rows_give_zero_and_neg_inf(h_q, num_sms):
     compare(out, lse, w, all_queries(w))
 
 
-def test_extra_cache_joint_softmax_and_extra_only_rows():
+@pytest.mark.parametrize("h_q", [16, 64, 128])
+def test_extra_cache_joint_softmax_and_extra_only_rows(h_q):
+    """One softmax over the FP8 main cache and the FP4 extra cache; a row
+    attended through the extra cache alone.  128 heads with an extra cache
+    run as two 64-head groups on the swap-AB kernel."""
     rng = np.random.default_rng(8)
     idx = _random_idx(rng, 3, 1, 256, 512, neg=0.05)
     xidx = _random_idx(rng, 3, 1, 130, 192, neg=0.05)
     idx[2] = -1                    # this row is attended through the extra cache alone
-    w = _custom(64, 256, 512, idx, xpool=192, xidx=xidx)
+    w = _custom(h_q, 256, 512, idx, xpool=192, xidx=xidx)
     out, lse, err = DeviceWorkload(w).run()
     assert err == 0
     compare(out, lse, w, all_queries(w))
