@@ -86,6 +86,20 @@ def _random_idx(rng, b, s, topk, pool, neg=0.0):
     return idx
 
 
+@pytest.mark.parametrize("h_q", [16, 32, 128])
+@pytest.mark.parametrize("num_sms", [0, 7])
+def test_three_query_tokens_per_sequence(h_q, num_sms):
+    """seq_len_q = 3 (odd), each query token of a sequence with its own
+    indices into the sequence's pool; 7 SMs give parts that cut query tokens
+    of different sequences."""
+    rng = np.random.default_rng(h_q + num_sms)
+    idx = _random_idx(rng, 3, 3, 300, 640, neg=0.02)
+    w = _custom(h_q, 300, 640, idx, s=3, seed=h_q)
+    out, lse, err = DeviceWorkload(w).run(num_sms=num_sms)
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
 @pytest.mark.parametrize("h_q", [16, 32, 64, 128])
 @pytest.mark.parametrize("topk", [1, 127, 129, 300])
 def test_heads_and_ragged_topk(h_q, topk):
