@@ -96,8 +96,8 @@ Plan make_plan(const mla_problem_t* p, int num_sms) {
 // cache; every other shape runs on the swap-AB kernel.
 bool uses_pair_kernel(const mla_problem_t* problem) { return problem->h_q == 128 && problem->extra_topk == 0; }
 
-// Where the 128-head kernel writes the fused epilogue's FP8 records of
-// query tokens that have one split.
+// Where the decode kernels write the fused epilogue's FP8 records of query
+// tokens that have one split.
 struct RopeOut {
   uint8_t* out;
   const int32_t* positions;
@@ -107,15 +107,14 @@ struct RopeOut {
 }  // namespace
 
 // Validation and the decode kernel's launch, shared by the bf16 and the
-// FP8 output calls.  With force_partials every query token's result goes
-// to the workspace (out may then be null); with rope (128-head kernel only)
-// query tokens of one split are written as FP8 records there instead of to
-// out; *pout receives the parameters.
+// FP8 output calls.  With rope, query tokens of one split are written as FP8
+// records there instead of to out (which may then be null); *pout receives
+// the parameters.
 mla_status_t decode_launch(const mla_problem_t* problem, const void* q, const void* kv, const int32_t* indices,
                            const void* extra_kv, const int32_t* extra_indices, const int32_t* d_sched,
                            const int32_t* d_num_splits, int32_t num_parts, void* workspace, size_t workspace_bytes,
-                           uint16_t* out, float* lse, int32_t* d_error, bool force_partials, const RopeOut* rope,
-                           mla_stream_t stream, DecodeParams* pout) {
+                           uint16_t* out, float* lse, int32_t* d_error, const RopeOut* rope, mla_stream_t stream,
+                           DecodeParams* pout) {
   mla_status_t st = validate_problem(problem);
   if (st != MLA_OK) return st;
   if (q == nullptr || kv == nullptr || indices == nullptr || d_sched == nullptr || d_num_splits == nullptr ||
@@ -167,7 +166,6 @@ mla_status_t decode_launch(const mla_problem_t* problem, const void* q, const vo
                                                                           : cap)
                        : 0;
   p.scale_log2 = problem->sm_scale * 1.4426950408889634f;
-  p.force_partials = force_partials ? 1 : 0;
   if (rope != nullptr) {
     p.rope_out = rope->out;
     p.positions = rope->positions;
@@ -240,7 +238,7 @@ mla_status_t mla_sparse_decode(const mla_problem_t* problem, const void* q, cons
   if (out == nullptr || !aligned16(out)) return MLA_ERR_INVALID_ARG;
   DecodeParams p{};
   st = decode_launch(problem, q, kv, indices, extra_kv, extra_indices, d_sched, d_num_splits, num_parts, workspace,
-                     workspace_bytes, static_cast<uint16_t*>(out), lse, d_error, false, nullptr, stream, &p);
+                     workspace_bytes, static_cast<uint16_t*>(out), lse, d_error, nullptr, stream, &p);
   if (st != MLA_OK) return st;
   if (num_parts > 1) {
     // Only query tokens with more than one split have partials to merge: a
@@ -271,15 +269,14 @@ mla_status_t mla_sparse_decode_rope_fp8(const mla_problem_t* problem, const void
   ro.out = static_cast<uint8_t*>(out_fp8);
   ro.positions = positions;
   for (int j = 0; j < 32; ++j) ro.freqs.f[j] = std::pow(static_cast<double>(rope_theta), -2.0 * j / 64.0);
-  // The 128-head kernel writes the records of one-split query tokens
-  // itself; the other kernel sends every token through the workspace.
-  const bool direct = uses_pair_kernel(problem);
+  // The decode kernels write the records of one-split query tokens
+  // themselves; only split tokens go through the workspace to the merge.
   DecodeParams p{};
   st = decode_launch(problem, q, kv, indices, extra_kv, extra_indices, d_sched, d_num_splits, num_parts, workspace,
-                     workspace_bytes, nullptr, lse, d_error, !direct, direct ? &ro : nullptr, stream, &p);
+                     workspace_bytes, nullptr, lse, d_error, &ro, stream, &p);
   if (st != MLA_OK) return st;
-  if (launch_rope_fp8(d_num_splits, p.ws_o, p.ws_lse, positions, ro.freqs, ro.out, lse, p.nq, problem->h_q, direct,
-                      direct && num_parts < p.nq ? d_sched : nullptr, num_parts, p.T,
+  if (launch_rope_fp8(d_num_splits, p.ws_o, p.ws_lse, positions, ro.freqs, ro.out, lse, p.nq, problem->h_q, true,
+                      num_parts < p.nq ? d_sched : nullptr, num_parts, p.T,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;

@@ -308,7 +308,10 @@ __device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTi
   }
 }
 
-template <int NH>
+// kRope: query tokens of one split leave as FP8 records after the
+// conjugate rotary embedding (the fused epilogue) instead of bf16 rows; a
+// separate instantiation, so that the bf16 kernel carries none of it.
+template <int NH, bool kRope>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap q_map) {
   using L = Smem<NH>;
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
       const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
       const int64_t split = static_cast<int64_t>(p.num_splits[qidx]) + local;
-      const bool direct = nsplit == 1 && !p.force_partials;
+      const bool direct = nsplit == 1;
       const bool split_ok = direct || (split >= 0 && split < p.ws_splits_cap && local < nsplit);
       if (i < NH) {
         const float l = red[i] + red[NH + i] + red[2 * NH + i] + red[3 * NH + i];
@@ -701,6 +704,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!split_ok && i == 0 && p.d_error) atomicOr(p.d_error, MLA_DEVERR_BAD_METADATA);
       named_bar_sync(1, kSoftmaxThreads);
+      if constexpr (kRope) {
+        if (direct) {
+          // The fused epilogue's records: dim d of every head's row.  The
+          // 32 lanes of a warp hold one 32-dim block (its e8m0 scale is the
+          // warp's maximum); dims 448..511 (quarter 3, warps 2 and 3) pair
+          // even and odd lanes for the conjugate rotation, each pair's angle
+          // taken once per lane pair.  The arithmetic of the merge kernel's
+          // fused epilogue, so the bytes agree.
+#pragma unroll 1
+          for (int r = 0; r < 4; ++r) {
+            const int d = r * 128 + i;
+            const bool rot = d >= 448;  // uniform in the warp
+            float cs = 1.f, sn = 0.f;
+            if (rot) rope_cos_sin(static_cast<double>(p.positions[qidx]), p.rope.f[(d - 448) >> 1], cs, sn);
+#pragma unroll 1
+            for (int c = 0; c < NH / 16; ++c) {
+              uint32_t o[16];
+              tmem_ld16(tO + r * NH + c * 16, o);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const int h = c * 16 + k;
+                float v = __uint_as_float(o[k]) * sm_linv[h];
+                if (rot) {
+                  const float w = __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+                  float a = (lane & 1) ? w : v, b = (lane & 1) ? v : w;
+                  rope_conj_apply(a, b, cs, sn);
+                  v = (lane & 1) ? b : a;
+                }
+                float amax = fabsf(v);
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o2));
+                const int ex = fp8_block_exponent(amax);
+                uint8_t* rec = p.rope_out + (static_cast<int64_t>(qidx) * p.h_q + hg * NH + h) * 528;
+                rec[d] = static_cast<uint8_t>(e4m3x2(ldexpf(v, -ex), 0.f) & 0xFFu);
+                if (lane == 0) rec[512 + (d >> 5)] = static_cast<uint8_t>(127 + ex);
+              }
+            }
+          }
+          tc_fence_before();
+          named_bar_sync(1, kSoftmaxThreads);  // O and sm_m reads done before the next token's tiles
+          ++n_seg;
+          continue;
+        }
+      }
 #pragma unroll 1
       for (int r = 0; r < 4; ++r) {
         const int d = r * 128 + i;
@@ -750,8 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int NH>
 cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) {
   constexpr int smem = Smem<NH>::kAlloc;
-  static std::atomic<uint64_t> configured{0};
-  cudaError_t e0 = max_dynamic_smem_once(configured, reinterpret_cast<const void*>(sparse_decode_kernel<NH>), smem);
+  const bool rope = p.rope_out != nullptr;
+  static std::atomic<uint64_t> configured{0}, configured_rope{0};
+  cudaError_t e0 =
+      rope ? max_dynamic_smem_once(configured_rope, reinterpret_cast<const void*>(sparse_decode_kernel<NH, true>), smem)
+           : max_dynamic_smem_once(configured, reinterpret_cast<const void*>(sparse_decode_kernel<NH, false>), smem);
   if (e0 != cudaSuccess) return e0;
   // Q viewed as [nq * h_q rows][512 bf16]; a box is NH rows x 64 dims, 128-byte swizzled.
   EncodeTiledFn enc = tensor_map_encoder();
@@ -765,7 +815,10 @@ cudaError_t launch_decode(const DecodeParams& p, int grid, cudaStream_t stream) 
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  sparse_decode_kernel<NH><<<grid, kThreads, smem, stream>>>(p, q_map);
+  if (rope)
+    sparse_decode_kernel<NH, true><<<grid, kThreads, smem, stream>>>(p, q_map);
+  else
+    sparse_decode_kernel<NH, false><<<grid, kThreads, smem, stream>>>(p, q_map);
   return cudaGetLastError();
 }
 

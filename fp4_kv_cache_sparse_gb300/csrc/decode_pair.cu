@@ -912,7 +912,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int nsplit = p.num_splits[qidx + 1] - p.num_splits[qidx];
       const int local = seg_begin == span.g_begin ? span.first_local_split : 0;
       const int64_t split = static_cast<int64_t>(p.num_splits[qidx]) + local;
-      const bool direct = nsplit == 1 && !p.force_partials;
+      const bool direct = nsplit == 1;
       const bool split_ok = direct || (split >= 0 && split < p.ws_splits_cap && local < nsplit);
       if (c == 0 && ch == 0) {
         const float lse = lt > 0.f ? (m + lg2_approx(lt)) * 0.6931471805599453f : -INFINITY;

@@ -36,10 +36,9 @@ struct DecodeParams {
   int nq, h_q, n_hg, topk, xtopk, Tm, T;
   int64_t pool_tokens, xpool_tokens;
   float scale_log2;         // sm_scale * log2(e)
-  int force_partials;       // 1: every query token's result goes to the workspace (a later kernel finishes it)
   // Fused output epilogue written by the decode kernel itself for query
-  // tokens of one split (128-head kernel only): null, or [nq][h_q][528]
-  // FP8 records after the conjugate rotary embedding at positions[qidx].
+  // tokens of one split: null, or [nq][h_q][528] FP8 records after the
+  // conjugate rotary embedding at positions[qidx].
   uint8_t* rope_out;
   const int32_t* positions;
   RopeFreqs rope;
