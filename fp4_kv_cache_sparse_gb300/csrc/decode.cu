@@ -136,6 +136,11 @@ __device__ __forceinline__ uint2 ldg_stream8(const uint8_t* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
+__device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) {
   uint32_t v;
   asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -286,7 +291,9 @@ struct QuarterRegs {
 };
 
 // seg = 16-dim segment of the lane within the quarter (0..7): dims
-// 128 qq + 16 seg .. +15.
+// 128 qq + 16 seg .. +15.  kFp8Scale: the quarter's FP8 scale word is loaded
+// here (otherwise load_scales_fp8 loads all four quarters' at once).
+template <bool kFp8Scale>
 __device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTile& lt, int qq, int seg,
                                              QuarterRegs& q) {
 #pragma unroll
@@ -298,13 +305,34 @@ __device__ __forceinline__ void load_quarter(const DecodeParams& p, const LaneTi
     } else if (!lt.extra) {
       const uint8_t* rec = p.kv + static_cast<int64_t>(id) * kRecFp8;
       q.data[r] = ldg_stream16(rec + qq * 128 + seg * 16);
-      q.scale[r] = ldg_u32(rec + 512 + qq * 4);
+      if constexpr (kFp8Scale) q.scale[r] = ldg_u32(rec + 512 + qq * 4);
     } else {
       const uint8_t* rec = p.xkv + static_cast<int64_t>(id) * kRecFp4;
       const uint2 d = ldg_stream8(rec + qq * 64 + seg * 8);
       q.data[r] = make_uint4(d.x, d.y, 0, 0);
       q.scale[r] = ldg_u8(rec + 256 + qq * 8 + seg);
     }
+  }
+}
+
+// FP8 tiles: the 16 scale bytes of each of the lane's rows in one load; word
+// qq goes to quarter qq's registers.  Called once the current tile's last
+// quarter has been stored (every quarter's scale registers are free then).
+// With 64 heads this replaces four 4-byte loads per row (fp8_b64_h64 80.9 ->
+// 76.9 us); with 16 heads the next tile's first quarter follows too soon
+// for loads issued this late (long_dense_b32_h16 482 -> 526 us), so fewer
+// heads keep the per-quarter loads.
+__device__ __forceinline__ void load_scales_fp8(const DecodeParams& p, const LaneTile& lt, QuarterRegs (&buf)[4]) {
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int32_t id = lt.id[r];
+    const uint4 s = id >= 0 ? ldg_u4(p.kv + static_cast<int64_t>(id) * kRecFp8 + 512)
+                            : make_uint4(127u * 0x01010101u, 127u * 0x01010101u, 127u * 0x01010101u,
+                                         127u * 0x01010101u);
+    buf[0].scale[r] = s.x;
+    buf[1].scale[r] = s.y;
+    buf[2].scale[r] = s.z;
+    buf[3].scale[r] = s.w;
   }
 }
 
@@ -384,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       off_odd[rr] = swz<128>(row * 128 + (2 * s4 + 1) * 16);
     }
     const int sshift = 8 * (2 * c1 + (s4 >> 1));  // scale byte within the quarter's scale word
+    constexpr bool kScalePerQuarter = NH < 64;
 
     uint32_t n_tile = 0, n_seg = 0;
     int64_t g = span.g_begin;
@@ -394,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       validate(p, cur, flag_bad);
       if (g + 1 < span.g_end) nxt = lane_tile(p, static_cast<int>(g + 1), row0);
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) load_quarter(p, cur, qq, seg, buf[qq]);
+      for (int qq = 0; qq < 4; ++qq) load_quarter<kScalePerQuarter>(p, cur, qq, seg, buf[qq]);
+      if (!kScalePerQuarter && !cur.extra) load_scales_fp8(p, cur, buf);
     }
     int64_t seg_end = g;  // forces a segment start on the first tile
     for (; g < span.g_end; ++g, ++n_tile) {
@@ -454,7 +484,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kQuarterFull + qq]);
         // The registers of this quarter now take the next tile's bytes.
-        if (g + 1 < span.g_end) load_quarter(p, nxt, qq, seg, buf[qq]);
+        if (g + 1 < span.g_end) {
+          if (!kScalePerQuarter && qq == 3 && !nxt.extra) load_scales_fp8(p, nxt, buf);
+          load_quarter<kScalePerQuarter>(p, nxt, qq, seg, buf[qq]);
+        }
       }
       cur = nxt;
       nxt = nxt2;
