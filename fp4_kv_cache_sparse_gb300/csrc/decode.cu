@@ -124,9 +124,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Record bytes: read once, so not kept in L1; the L2 fetches the 256-byte
+// block around each piece, which holds the neighbouring pieces of the same
+// record that later quarters read (a 128-byte quarter slice straddles lines).
 __device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
