@@ -187,6 +187,47 @@ def test_large_scores_exercise_rescaling():
     compare(out, lse, w, all_queries(w))
 
 
+@pytest.mark.parametrize("h_q", [16, 64, 128])
+def test_large_block_scales_in_the_decode(h_q):
+    """FP8 block scales beyond 2^15 (scale bytes above 142, which the
+    dequantization takes in two multiplies) through each decode kernel's own
+    scale handling: per-quarter loads (16 heads), per-tile loads (64 heads)
+    and the 128-head kernel's staged scales.  Multiplying every latent by
+    2^24 leaves the E4M3 codes as they are and raises each scale byte by 24;
+    with the queries multiplied by 2^-24 the scores do not change.  So the
+    scaled problem must give exactly 2^24 times the outputs and the same LSE
+    as the unscaled one, which is checked against the oracle.  Half the
+    latents are 2^-16 smaller, so that scaled warps see both dequantization
+    paths."""
+    rng = np.random.default_rng(31 + h_q)
+    b, topk, pool = 2, 1024, 4096
+    idx = _random_idx(rng, b, 1, topk, pool, neg=0.01)
+    pos = np.unique(idx[idx >= 0])
+    data = rng.standard_normal((pos.shape[0], 512), dtype=np.float32)
+    data *= np.where(rng.random(pos.shape[0]) < 0.5, 1.0, 2.0 ** -16).astype(np.float32)[:, None]
+    rec_small = synth.encode_fp8_records(data)
+    rec_big = synth.encode_fp8_records(data * np.float32(2.0 ** 24))
+    assert np.array_equal(rec_small[:, :512], rec_big[:, :512])
+    assert np.array_equal(rec_small[:, 512:].astype(np.int32) + 24, rec_big[:, 512:].astype(np.int32))
+    assert (rec_small[:, 512:] <= 142).all()
+    assert (rec_big[:, 512:] > 142).any() and (rec_big[:, 512:] <= 142).any()
+    q = rng.standard_normal((b, 1, h_q, 512), dtype=np.float32)
+    cfg = synth.Config(99, "custom", b, 1, h_q, pool, topk)
+
+    def run(rec, qs):
+        w = synth.Workload(cfg=cfg, q_bits=synth.f32_to_bf16_bits(qs), idx=idx.astype(np.int32),
+                           pool_tokens=pool * b, ref_pos=pos.astype(np.int64), ref_rec=rec)
+        out, lse, err = DeviceWorkload(w).run()
+        assert err == 0
+        return w, out, lse
+
+    w, out_s, lse_s = run(rec_small, q)
+    _, out_b, lse_b = run(rec_big, q * np.float32(2.0 ** -24))
+    compare(out_s, lse_s, w, all_queries(w))
+    assert torch.equal(out_b.float(), out_s.float() * 2.0 ** 24)
+    assert torch.equal(lse_b, lse_s)
+
+
 @pytest.mark.parametrize("h_q", [64, 128])
 def test_growing_scores_move_the_max_every_tile(h_q):
     """Every query row shares a component along one unit direction u, and the
