@@ -26,7 +26,9 @@
 // its inputs are ready (O += P V as one 128x256x16 product per 16 tokens).  Records reach shared memory by TMA row gathers
 // (tile::gather4, 4 tokens per instruction, 256 bytes of a record per row)
 // into a 3-slot staging ring, so the dequantizing warps never have global
-// loads in flight when they publish a slot.
+// loads in flight when they publish a slot.  Outputs (and split partials)
+// leave by TMA tensor stores of 32-row x 32-dim blocks staged in the idle P
+// buffers.
 //
 // Warps: 0-7 softmax (two per TMEM lane quadrant, one per 16-token column
 // half of the quarter), 8-11 dequant, 12 loader (indices, validity mask,
@@ -118,6 +120,17 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_peer, const void* src,
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Waits until every bulk group of this thread has completed (writes included).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Tiled TMA store of a shared-memory box to global coordinates (x, y).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -128,13 +141,6 @@ __device__ __forceinline__ void ldg_v8(const void* p, uint32_t* r) {
   asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "l"(p));
-}
-
-// 32 bytes to global memory; p must be 32-byte aligned.
-__device__ __forceinline__ void stg_v8(void* p, const uint4& a, const uint4& b) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
-               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
-               : "memory");
 }
 
 // Non-blocking test of a phase's completion.
@@ -265,7 +271,8 @@ __device__ __forceinline__ PSpan pair_span(const DecodeParams& p, int part) {
 // separate instantiation, so that the bf16 kernel carries none of it.
 template <bool kRope>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
-    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kv_map) {
+    sparse_decode_pair_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kv_map,
+                              const __grid_constant__ CUtensorMap out_map, const __grid_constant__ CUtensorMap ws_map) {
   using L = PairSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -657,9 +664,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // aligned the row goes in 32-byte loads (half the requests of 16-byte
     // ones); otherwise in 16-byte loads.
     const bool q_al32 = (reinterpret_cast<uintptr_t>(p.q) & 31) == 0;
-    // Likewise the O rows out: 32-byte stores when the destination allows.
-    const bool out_al32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
-    const bool ws_al32 = (reinterpret_cast<uintptr_t>(p.ws_o) & 31) == 0;
     // FP8 records (528 bytes, a multiple of 16) in 16-byte pieces when the
     // destination allows, else in 4-byte words.
     const bool rope_al16 = (reinterpret_cast<uintptr_t>(p.rope_out) & 15) == 0;
@@ -938,9 +942,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       tc_fence_after();
       // O rows leave through this warp's 4 KB of the P buffers (idle now:
       // every PV of this token is done, and the peer sends its next P only
-      // after this CTA's next partial scores), so that the global stores go
-      // out as whole row pieces: 64 bytes of one bf16 row or 128 bytes of
-      // one fp32 row per group of lanes (32 bytes per lane when aligned).
+      // after this CTA's next partial scores): each 32-dim block of the
+      // warp's 32 rows is staged there and written by one TMA store.
       uint8_t* ost = sP + warp * 4096;
       // The fused epilogue's records: this lane's head row, bytes d0 .. d0+31
       // and scale byte 512 + d0 / 32 for each 32-dim block d0 of this warp.
@@ -995,53 +998,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           }
         }
         if (direct) {
+          // TMA stores: the 32 x 64-byte block goes out as one tiled store
+          // (the staging block's 64-byte swizzle is the tensor map's), from
+          // two staging halves in turn.
+          uint8_t* st = ost + (j & 1) * 2048;
+          if (j >= 2) {
+            if (lane == 0) bulk_wait_read_1();  // the store of block j - 2 has read this half
+            __syncwarp();
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(ost + swz<64>(lane * 64 + u * 16)) =
+            *reinterpret_cast<uint4*>(st + swz<64>(lane * 64 + u * 16)) =
                 make_uint4(pack_bf16x2(__uint_as_float(o[8 * u + 0]) * linv, __uint_as_float(o[8 * u + 1]) * linv),
                            pack_bf16x2(__uint_as_float(o[8 * u + 2]) * linv, __uint_as_float(o[8 * u + 3]) * linv),
                            pack_bf16x2(__uint_as_float(o[8 * u + 4]) * linv, __uint_as_float(o[8 * u + 5]) * linv),
                            pack_bf16x2(__uint_as_float(o[8 * u + 6]) * linv, __uint_as_float(o[8 * u + 7]) * linv));
+          fence_proxy_async_smem();
           __syncwarp();
-          if (out_al32) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int r = 16 * k + (lane >> 1), h = lane & 1;  // row of this warp, 32-byte piece
-              const uint4 a = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + (2 * h) * 16));
-              const uint4 b = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + (2 * h + 1) * 16));
-              stg_v8(p.out + (static_cast<int64_t>(qidx) * p.h_q + 32 * qd + r) * kD + d0 + 16 * h, a, b);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int r = 8 * k + (lane >> 2), u = lane & 3;  // row of this warp, 16-byte piece
-              const uint4 v = *reinterpret_cast<const uint4*>(ost + swz<64>(r * 64 + u * 16));
-              *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(qidx) * p.h_q + 32 * qd + r) * kD + d0 + 8 * u) =
-                  v;
-            }
+          if (lane == 0) {
+            tma_store_2d(&out_map, st, d0, qidx * p.h_q + 32 * qd);
+            bulk_commit();
           }
         } else if (split_ok) {
+          // The same for an fp32 partial: 32 x 128-byte blocks with the
+          // 128-byte swizzle, one staging block (4 KB) per warp.
+          if (j >= 1) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+          }
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<float4*>(ost + swz<128>(lane * 128 + u * 16)) =
                 make_float4(__uint_as_float(o[4 * u + 0]) * linv, __uint_as_float(o[4 * u + 1]) * linv,
                             __uint_as_float(o[4 * u + 2]) * linv, __uint_as_float(o[4 * u + 3]) * linv);
+          fence_proxy_async_smem();
           __syncwarp();
-          if (ws_al32) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int r = 8 * k + (lane >> 2), h = lane & 3;
-              const uint4 a = *reinterpret_cast<const uint4*>(ost + swz<128>(r * 128 + (2 * h) * 16));
-              const uint4 b = *reinterpret_cast<const uint4*>(ost + swz<128>(r * 128 + (2 * h + 1) * 16));
-              stg_v8(p.ws_o + (split * p.h_q + 32 * qd + r) * kD + d0 + 8 * h, a, b);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int r = 4 * k + (lane >> 3), u = lane & 7;
-              const float4 v = *reinterpret_cast<const float4*>(ost + swz<128>(r * 128 + u * 16));
-              *reinterpret_cast<float4*>(p.ws_o + (split * p.h_q + 32 * qd + r) * kD + d0 + 4 * u) = v;
-            }
+          if (lane == 0) {
+            tma_store_2d(&ws_map, ost, d0, static_cast<int>(split) * p.h_q + 32 * qd);
+            bulk_commit();
           }
         }
         __syncwarp();  // this warp's staging block is rewritten next
@@ -1051,12 +1045,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       // No warp sends the next partial scores (after which the peer's next P
       // lands here) or writes the next P before every warp's O rows have
-      // been read out of the P buffers.
+      // been read out of the P buffers (by the TMA stores too).
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
       named_bar_sync(1, kSoftThreads);
       tc_fence_before();
       ++n_seg;
     }
-    if (lane == 0) bulk_wait_read();  // this warp's last copies out of shared memory
+    // This warp's last copies out of shared memory, and the TMA stores'
+    // writes, are complete.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1096,10 +1095,35 @@ cudaError_t launch_decode_pair(const DecodeParams& p, int num_parts, cudaStream_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // Outputs and split partials leave by TMA stores: out as [rows][512] bf16,
+  // the partials as [rows][512] fp32, in boxes of 32 rows x 32 dims (both
+  // buffers are 16-byte aligned, as the entry points check).  A map that is
+  // not needed (no bf16 output, no workspace) stays a copy of kv_map.
+  CUtensorMap out_map = kv_map, ws_map = kv_map;
+  if (p.out != nullptr) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.nq) * p.h_q};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&out_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (p.ws_o != nullptr && p.ws_splits_cap > 0) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.ws_splits_cap) * p.h_q};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&ws_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.ws_o, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   if (rope)
-    sparse_decode_pair_kernel<true><<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map);
+    sparse_decode_pair_kernel<true><<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map, out_map, ws_map);
   else
-    sparse_decode_pair_kernel<false><<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map);
+    sparse_decode_pair_kernel<false><<<2 * num_parts, kPThreads, smem, stream>>>(p, kv_map, out_map, ws_map);
   return cudaGetLastError();
 }
 

@@ -146,10 +146,10 @@ mla_status_t mla_get_metadata(const mla_problem_t* problem, int32_t num_sms,
  * page_size != 64, num_kv_heads != 1, unsupported h_q -> MLA_ERR_UNSUPPORTED.
  * Split partials are merged by an internal launch of the combine kernel on
  * the same stream.  Calls that share a workspace must not overlap.
- * Alignment beyond the minimum: with q, out and workspace 32-byte aligned
- * (any allocator's default), the 128-head kernel moves the query rows and
- * the outputs in 32-byte pieces; at 16 bytes it uses 16-byte pieces, with
- * identical results.
+ * out and workspace must be 16-byte aligned (MLA_ERR_INVALID_ARG otherwise).
+ * Alignment beyond the minimum: with q 32-byte aligned (any allocator's
+ * default), the 128-head kernel loads the query rows in 32-byte pieces; at
+ * 16 bytes it uses 16-byte pieces, with identical results.
  */
 mla_status_t mla_sparse_decode(const mla_problem_t* problem,
                                const void* q, const void* kv, const int32_t* indices,

@@ -317,11 +317,12 @@ def _off16(shape, dtype, dev):
 
 
 def test_alignment_paths_agree():
-    """q, out and the workspace only 16-byte aligned (the contract's minimum)
-    take the kernel's 16-byte load and store paths; 32-byte aligned buffers
-    the 32-byte ones: both give the same bits, and both match the oracle
-    (one query token's tiles are split over many parts, so the workspace
-    path runs too)."""
+    """q, out and the workspace only 16-byte aligned (the contract's minimum):
+    q takes the 128-head kernel's 16-byte load path instead of the 32-byte
+    one, and the outputs and split partials leave by TMA stores from either
+    base.  Both give the same bits, and both match the oracle (one query
+    token's tiles are split over many parts, so the workspace path runs
+    too)."""
     w = synth.make_workload(2, batch=1, workers=1)
     dw = DeviceWorkload(w)
     dec = dw.decoder()
