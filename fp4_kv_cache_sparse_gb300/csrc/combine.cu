@@ -7,7 +7,10 @@
 // each lane accumulating 16 of the 512 dims from float4 loads that are all
 // issued before any is used.  Blocks of four warps at no more than 73
 // registers a thread (seven blocks a SM), so that the rows of a 64-query,
-// 64-head batch are all resident at once.
+// 64-head batch are all resident at once.  In the grid over the decode's
+// parts (a block = four heads of one split query token, which then has at
+// most two splits) the block's partial rows come by bulk copies into shared
+// memory, issued before the LSE loads.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -111,6 +114,80 @@ __device__ __forceinline__ int64_t merge_row_of(const int32_t* __restrict__ sche
   return q * T >= g0 ? q : -1;
 }
 
+// The by-part grid's merge of one split query token for the block's four
+// heads: their partial rows of each split (4 x 2 KB, contiguous) arrive by
+// one bulk copy per split into shared memory, issued before the LSE loads so
+// that the two overlap.  Returns false (nothing done) when there are more
+// splits than the staging holds.
+constexpr int kStageSplits = 2;
+__device__ __forceinline__ bool merge_rows_staged(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                                                  int s0, int n, int h0, int h_q, float (&acc)[16], float& L) {
+  __shared__ alignas(128) float stage[kStageSplits][kWarps * 512];
+  __shared__ alignas(8) uint64_t bar;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (n > kStageSplits) return false;
+  const int nh = min(kWarps, h_q - h0);
+  const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(n * nh * 2048) : "memory");
+    for (int i = 0; i < n; ++i)
+      asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                       static_cast<uint32_t>(__cvta_generic_to_shared(&stage[i][0]))),
+                   "l"(o_part + (static_cast<int64_t>(s0 + i) * h_q + h0) * 512), "r"(nh * 2048), "r"(b)
+                   : "memory");
+  }
+  __syncthreads();
+  const int h = h0 + warp;
+  const float* lrow = lse_part + static_cast<int64_t>(s0) * h_q + h;
+  const float li = lane < n ? lrow[static_cast<int64_t>(lane) * h_q] : -INFINITY;
+  const float M = warp_max(li);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float wl = 0.f;
+  if (M != -INFINITY) {
+    const float z = li == -INFINITY ? 0.f : expf(li - M);
+    L = M + logf(warp_sum(z));
+    wl = li == -INFINITY ? 0.f : expf(li - L);
+  } else {
+    L = -INFINITY;
+  }
+  // The copies land (bounded wait: 2 s of global time, then the block goes
+  // on; they cannot fail short of a fault).
+  {
+    uint32_t ok = 0;
+    uint64_t t0 = 0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(b)
+          : "memory");
+      if (ok) break;
+      uint64_t t1;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+      if (t1 - t0 > 2000000000ull) break;
+    }
+  }
+  if (M == -INFINITY || warp >= nh) return true;
+  for (int i = 0; i < n; ++i) {
+    const float w = __shfl_sync(kFull, wl, i);
+    if (w == 0.f) continue;
+    const float4* src = reinterpret_cast<const float4*>(&stage[i][warp * 512]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = src[k * 32 + lane];
+      acc[4 * k + 0] += w * v.x;
+      acc[4 * k + 1] += w * v.y;
+      acc[4 * k + 2] += w * v.z;
+      acc[4 * k + 3] += w * v.w;
+    }
+  }
+  return true;
+}
+
 template <bool kByPart>
 __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* __restrict__ num_splits,
                                                              const float* __restrict__ o_part,
@@ -132,7 +209,11 @@ __global__ void __launch_bounds__(kWarps * 32, 7) combine_kernel(const int32_t* 
   const int n = num_splits[qidx + 1] - s0;
   if (skip_single && n == 1) return;
   float acc[16];
-  const float L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
+  float L;
+  bool staged = false;
+  if constexpr (kByPart)
+    staged = merge_rows_staged(o_part, lse_part, s0, n, static_cast<int>(blockIdx.y) * kWarps, h_q, acc, L);
+  if (!staged) L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
   uint2* dst = reinterpret_cast<uint2*>(out + row * 512);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -175,7 +256,11 @@ __global__ void __launch_bounds__(kWarps * 32, 4) rope_fp8_kernel(const int32_t*
   const int n = num_splits[qidx + 1] - s0;
   if (skip_single && n == 1) return;  // written by the decode kernel itself
   float acc[16];
-  const float L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
+  float L;
+  bool staged = false;
+  if constexpr (kByPart)
+    staged = merge_rows_staged(o_part, lse_part, s0, n, static_cast<int>(blockIdx.y) * kWarps, h_q, acc, L);
+  if (!staged) L = merge_row(o_part, lse_part, s0, n, h, h_q, lane, acc);
   if (lane >= 16) {
     const double pos = static_cast<double>(positions[qidx]);
 #pragma unroll
