@@ -160,6 +160,24 @@ def test_duplicate_indices_count_twice(h_q):
     compare(out, lse, w, all_queries(w))
 
 
+@pytest.mark.parametrize("h_q", [16, 64, 128])
+def test_first_and_last_pool_tokens(h_q):
+    """Indices naming token 0 and the pool's last token (the last row of the
+    128-head kernel's row-gather tensor, the last record the other kernel
+    loads), in the first and the last slot of a row whose last tile is
+    ragged, from both sequences."""
+    rng = np.random.default_rng(17)
+    b, topk, pool = 2, 300, 320
+    idx = _random_idx(rng, b, 1, topk, pool)
+    last = pool * b - 1
+    idx[0, 0, 0], idx[0, 0, topk - 1] = 0, last
+    idx[b - 1, 0, 0], idx[b - 1, 0, topk - 1] = last, 0
+    w = _custom(h_q, topk, pool, idx)
+    out, lse, err = DeviceWorkload(w).run()
+    assert err == 0
+    compare(out, lse, w, all_queries(w))
+
+
 @pytest.mark.parametrize("h_q", [32, 64, 128])
 def test_bad_indices_are_skipped_and_flagged(h_q):
     """Entries past the pool or negative other than -1 are skipped on both
